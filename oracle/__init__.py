@@ -1,0 +1,190 @@
+"""CPU oracle for paged decode/verify attention and speculative rejection sampling.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+product library (``verify_attention_spec_gb300``) never imports it, links it or
+falls back to it; the two share no code.
+
+The arithmetic lives in ``oracle.c`` (plain C, IEEE double, OpenMP over independent
+rows); this module only builds it with gcc and marshals numpy arrays through ctypes.
+Every function cites the passage it follows in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, F64 = 0, 1, 2
+OK, E_ARG, E_PAGE, E_LEN, E_TOKEN, E_DIST = 0, -1, -2, -3, -4, -5
+
+# Decisions whose uniform lies within this distance of its threshold are flagged
+# (the tolerance the spec states for accepted lengths and emitted tokens).
+FLAG_WINDOW = 1e-6
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (portable flags, no FMA contraction)."""
+    with _lock:
+        if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+            return _LIB
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+        return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    i32, i64, u64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_double
+    lib.oracle_paged_attn.argtypes = [P, P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32,
+                                      i32, dbl, P, P]
+    lib.oracle_paged_attn.restype = i32
+    lib.oracle_philox4x32_10.argtypes = [P, P, P]
+    lib.oracle_philox4x32_10.restype = None
+    lib.oracle_philox4x32_10_many.argtypes = [P, i64, P, P]
+    lib.oracle_philox4x32_10_many.restype = None
+    lib.oracle_uniforms.argtypes = [u64, i32, i32, P, P]
+    lib.oracle_uniforms.restype = None
+    lib.oracle_spec_verify_given_uniforms.argtypes = [P, P, P, P, P, i32, i32, i32, dbl, P, P,
+                                                      P, P, P]
+    lib.oracle_spec_verify_given_uniforms.restype = i32
+    lib.oracle_spec_verify.argtypes = [P, P, P, u64, i32, i32, i32, dbl, P, P, P, P, P]
+    lib.oracle_spec_verify.restype = i32
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _as_storage(x: np.ndarray, dtype_code: int) -> np.ndarray:
+    if dtype_code == F32:
+        return np.ascontiguousarray(x, dtype=np.float32)
+    if dtype_code == BF16:
+        return np.ascontiguousarray(x, dtype=np.uint16)  # raw bf16 bit patterns
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def paged_attn(q, k_pages, v_pages, block_table, seq_lens, query_lens, *, dtype_code: int,
+               scale: float | None = None):
+    """Float64 paged attention (oracle.c: oracle_paged_attn).
+
+    q: [total_q_tokens, Hq, D]; k_pages/v_pages: [num_pages, page_size, Hkv, D], given as
+    float32, raw bf16 bits (uint16) or float64 according to ``dtype_code``.
+    Returns (out float64 [total_q_tokens, Hq, D], lse float64 [total_q_tokens, Hq]).
+    """
+    lib = _load()
+    q = _as_storage(q, dtype_code)
+    k_pages = _as_storage(k_pages, dtype_code)
+    v_pages = _as_storage(v_pages, dtype_code)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(query_lens, dtype=np.int32)
+    T, Hq, D = q.shape
+    num_pages, page_size, Hkv, D2 = k_pages.shape
+    assert D2 == D and v_pages.shape == k_pages.shape
+    B = sl.shape[0]
+    maxp = bt.shape[1] if bt.ndim == 2 else 0
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    lse = np.zeros((T, Hq), dtype=np.float64)
+    rc = lib.oracle_paged_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), dtype_code, _ptr(bt),
+                               _ptr(sl), _ptr(ql), B, Hq, Hkv, D, page_size, num_pages, maxp,
+                               float(scale), _ptr(out), _ptr(lse))
+    if rc != OK:
+        raise ValueError(f"oracle_paged_attn rejected its arguments (code {rc})")
+    return out, lse
+
+
+def philox4x32_10(counters: np.ndarray, key) -> np.ndarray:
+    """Philox4x32-10 of each 128-bit counter row [n, 4] (uint32) under key (k0, k1)."""
+    lib = _load()
+    ctr = np.ascontiguousarray(counters, dtype=np.uint32).reshape(-1, 4)
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros_like(ctr)
+    lib.oracle_philox4x32_10_many(_ptr(ctr), ctr.shape[0], _ptr(k), _ptr(out))
+    return out
+
+
+def uniforms(seed: int, B: int, k: int):
+    """The uniforms the rule consumes: r [B, k] and s [B, k+1] (oracle.c: oracle_uniforms)."""
+    lib = _load()
+    r = np.zeros((B, max(k, 0)), dtype=np.float64)
+    s = np.zeros((B, k + 1), dtype=np.float64)
+    lib.oracle_uniforms(ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), B, k, _ptr(r), _ptr(s))
+    return r, s
+
+
+class VerifyResult:
+    def __init__(self, accepted_len, out_tokens, margin, flag_pos, fallback, status):
+        self.accepted_len = accepted_len
+        self.out_tokens = out_tokens
+        self.margin = margin
+        self.flag_pos = flag_pos
+        self.fallback = fallback
+        self.status = status
+
+
+def _verify_buffers(B, k):
+    return (np.zeros(B, dtype=np.int32), np.zeros((B, k + 1), dtype=np.int32),
+            np.zeros(B, dtype=np.float64), np.zeros(B, dtype=np.int32),
+            np.zeros(B, dtype=np.int32))
+
+
+def spec_verify_given_uniforms(p, q, draft_tokens, r, s, flag_window: float = FLAG_WINDOW):
+    """Modified rejection sampling with explicit uniforms
+    (oracle.c: oracle_spec_verify_given_uniforms).  p [B,k+1,V], q [B,k,V] float32."""
+    lib = _load()
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    B, k1, V = p.shape
+    k = k1 - 1
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, k, V)
+    x = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, k)
+    r = np.ascontiguousarray(r, dtype=np.float64).reshape(B, k)
+    s = np.ascontiguousarray(s, dtype=np.float64).reshape(B, k + 1)
+    acc, out, mg, fp, fb = _verify_buffers(B, k)
+    rc = lib.oracle_spec_verify_given_uniforms(_ptr(p), _ptr(q), _ptr(x), _ptr(r), _ptr(s), B,
+                                               k, V, float(flag_window), _ptr(acc), _ptr(out),
+                                               _ptr(mg), _ptr(fp), _ptr(fb))
+    return VerifyResult(acc, out, mg, fp, fb, rc)
+
+
+def spec_verify(p, q, draft_tokens, seed: int, flag_window: float = FLAG_WINDOW):
+    """Philox uniforms + modified rejection sampling (oracle.c: oracle_spec_verify)."""
+    lib = _load()
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    B, k1, V = p.shape
+    k = k1 - 1
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, k, V)
+    x = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, k)
+    acc, out, mg, fp, fb = _verify_buffers(B, k)
+    rc = lib.oracle_spec_verify(_ptr(p), _ptr(q), _ptr(x),
+                                ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), B, k, V,
+                                float(flag_window), _ptr(acc), _ptr(out), _ptr(mg), _ptr(fp),
+                                _ptr(fb))
+    return VerifyResult(acc, out, mg, fp, fb, rc)

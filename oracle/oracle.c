@@ -1,0 +1,415 @@
+/*
+ * oracle.c -- plain, slow, obviously correct CPU reference for the hot path of one
+ * continuous-batching iteration: paged decode/verify attention and speculative
+ * rejection sampling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or calls
+ * this file; only the test-suite, the smoke check and the CPU-baseline leg of the
+ * benchmark do.  It shares no code, header, table or constant with the CUDA path.
+ *
+ * Precision: every quantity is computed in IEEE double from the exact input values
+ * (fp32 inputs widened, bf16 inputs decoded bit-exactly, fp64 inputs as given).
+ *
+ * Sources (the pages this follows):
+ *  - "Continuous Batching and Speculative Decoding: How Modern LLM Serving Engines
+ *    Actually Work" (syslabs.in), sections "PagedAttention: making the KV cache
+ *    schedulable" and "Speculative decoding" / "The core idea".
+ *  - "llm-inference-optimization-batching" (tempatgunting.com), section "Anatomy of
+ *    the KV Cache: Memory Layout, Paging and Quantization Trade-offs" (pool shape
+ *    [num_blocks, block_size, num_heads, head_dim], block table per sequence) and
+ *    section "Speculative Decoding: Turning Verification Parallelism into Latency
+ *    Wins" (accept/resample/bonus, rollback).
+ *  - "Continuous Batching & Speculative Decoding" (neuralmasteryai.com), section
+ *    "3. Mathematical Proof: Exact Distributional Match" / "The Modified Rejection
+ *    Sampling Algorithm" (accept iff r <= min(1, p/q); halt at the first rejection;
+ *    resample from max(0, p - q) normalised).
+ *  - Philox4x32-10: J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
+ *    Random Numbers: As Easy as 1, 2, 3", SC'11 (the published counter-based
+ *    generator; the pages only say "random()").
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *  - seq_lens[i] counts every KV token of sequence i, including this step's query
+ *    tokens; query token j of sequence i sits at absolute position L_i - ql_i + j and
+ *    attends to positions 0..that position (causal inside the draft window).
+ *  - query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ *  - lse is the natural log of sum_t exp(scale * q.k_t).
+ *  - acceptance uses "<=" (the neuralmasteryai page), evaluated as r*q <= p in double.
+ *  - uniforms: u = (word + 0.5) * 2^-32 from Philox4x32-10 with
+ *    counter = (position, sequence, 0, 0) and key = (seed low word, seed high word);
+ *    word 0 drives the ratio test at that position, word 1 the resample / bonus draw.
+ *  - inverse-CDF draw: emit the smallest x whose inclusive prefix sum exceeds s * S.
+ *  - a rejection whose residual sums to zero (impossible in exact arithmetic) falls
+ *    back to sampling from the target row p_j.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_F32 0
+#define ORC_BF16 1
+#define ORC_F64 2
+
+#define ORC_OK 0
+#define ORC_E_ARG (-1)
+#define ORC_E_PAGE (-2)
+#define ORC_E_LEN (-3)
+#define ORC_E_TOKEN (-4)
+#define ORC_E_DIST (-5)
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Element `idx` of an array of the given storage type, widened to double.
+ * bf16 is the top half of an fp32 bit pattern, so the decode is exact. */
+static double load_elem(const void* base, int dtype, size_t idx) {
+  if (dtype == ORC_F32) return (double)((const float*)base)[idx];
+  if (dtype == ORC_BF16) {
+    uint32_t bits = ((uint32_t)((const uint16_t*)base)[idx]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return ((const double*)base)[idx];
+}
+
+/* ------------------------------------------------------------------------------
+ * Paged attention, plain definition.
+ *
+ * Pool layout (tempatgunting.com, "Anatomy of the KV Cache"): k_pages and v_pages
+ * are [num_pages, page_size, num_kv_heads, head_dim]; block_table is
+ * [num_seqs, max_pages_per_seq]; logical position t of sequence i lives in physical
+ * page block_table[i][t / page_size], slot t % page_size (syslabs.in,
+ * "PagedAttention": a per-sequence table maps logical positions to blocks).
+ *
+ * q and out are [total_q_tokens, num_q_heads, head_dim], rows packed by sequence in
+ * order; lse is [total_q_tokens, num_q_heads].  For every query row:
+ *     s_t   = scale * <q, k_t>          for t = 0 .. pos
+ *     lse   = log sum_t exp(s_t)
+ *     out   = sum_t exp(s_t - lse) v_t
+ * Returns ORC_OK, or a negative code for arguments that make the result undefined.
+ * ---------------------------------------------------------------------------- */
+int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                      const int32_t* block_table, const int32_t* seq_lens,
+                      const int32_t* query_lens, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int page_size, int num_pages,
+                      int max_pages_per_seq, double scale, double* out, double* lse) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      page_size <= 0 || num_pages < 0 || max_pages_per_seq < 0)
+    return ORC_E_ARG;
+  if (num_q_heads % num_kv_heads != 0) return ORC_E_ARG;
+  if (dtype != ORC_F32 && dtype != ORC_BF16 && dtype != ORC_F64) return ORC_E_ARG;
+
+  /* First query row of every sequence: exclusive prefix sum of query_lens. */
+  int64_t* row0 = (int64_t*)malloc(sizeof(int64_t) * (size_t)(num_seqs + 1));
+  if (!row0) return ORC_E_ARG;
+  row0[0] = 0;
+  for (int i = 0; i < num_seqs; ++i) {
+    int L = seq_lens[i], ql = query_lens[i];
+    if (ql < 0 || L < 0 || ql > L || (int64_t)L > (int64_t)max_pages_per_seq * page_size) {
+      free(row0);
+      return ORC_E_LEN;
+    }
+    int npages = (L + page_size - 1) / page_size;
+    for (int pg = 0; pg < npages; ++pg) {
+      int32_t id = block_table[(size_t)i * max_pages_per_seq + pg];
+      if (id < 0 || id >= num_pages) {
+        free(row0);
+        return ORC_E_PAGE;
+      }
+    }
+    row0[i + 1] = row0[i] + ql;
+  }
+
+  const int group = num_q_heads / num_kv_heads;
+  const int64_t work = (int64_t)num_seqs * num_q_heads;
+
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t w = 0; w < work; ++w) {
+    const int i = (int)(w / num_q_heads);
+    const int h = (int)(w % num_q_heads);
+    const int g = h / group; /* KV head read by query head h */
+    const int L = seq_lens[i];
+    const int ql = query_lens[i];
+    if (ql == 0) continue;
+    double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    for (int j = 0; j < ql; ++j) {
+      const int pos = L - ql + j; /* absolute position of this query token */
+      const int64_t row = row0[i] + j;
+      const size_t qbase = ((size_t)row * num_q_heads + h) * head_dim;
+      double m = -INFINITY;
+      for (int t = 0; t <= pos; ++t) {
+        const int32_t page = block_table[(size_t)i * max_pages_per_seq + t / page_size];
+        const int slot = t % page_size;
+        const size_t kbase =
+            (((size_t)page * page_size + slot) * num_kv_heads + g) * head_dim;
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d)
+          dot += load_elem(q, dtype, qbase + d) * load_elem(k_pages, dtype, kbase + d);
+        s[t] = scale * dot;
+        if (s[t] > m) m = s[t];
+      }
+      double sum = 0.0;
+      for (int t = 0; t <= pos; ++t) sum += exp(s[t] - m);
+      const double row_lse = m + log(sum);
+      lse[(size_t)row * num_q_heads + h] = row_lse;
+      double* o = out + qbase;
+      for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+      for (int t = 0; t <= pos; ++t) {
+        const double wt = exp(s[t] - row_lse);
+        const int32_t page = block_table[(size_t)i * max_pages_per_seq + t / page_size];
+        const int slot = t % page_size;
+        const size_t vbase =
+            (((size_t)page * page_size + slot) * num_kv_heads + g) * head_dim;
+        for (int d = 0; d < head_dim; ++d) o[d] += wt * load_elem(v_pages, dtype, vbase + d);
+      }
+    }
+    free(s);
+  }
+  free(row0);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------
+ * Philox4x32-10 (Salmon et al., SC'11): ten rounds of the 4x32 Philox S-box on a
+ * 128-bit counter under a 64-bit key, the key advanced by the two Weyl constants
+ * between rounds.
+ * ---------------------------------------------------------------------------- */
+static void philox_sbox(uint32_t c[4], const uint32_t k[2]) {
+  const uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c[0];
+  const uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c[2];
+  const uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+  const uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+  const uint32_t n0 = hi1 ^ c[1] ^ k[0];
+  const uint32_t n2 = hi0 ^ c[3] ^ k[1];
+  c[0] = n0;
+  c[1] = lo1;
+  c[2] = n2;
+  c[3] = lo0;
+}
+
+void oracle_philox4x32_10(const uint32_t counter[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c[4] = {counter[0], counter[1], counter[2], counter[3]};
+  uint32_t k[2] = {key[0], key[1]};
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      k[0] += 0x9E3779B9u;
+      k[1] += 0xBB67AE85u;
+    }
+    philox_sbox(c, k);
+  }
+  out[0] = c[0];
+  out[1] = c[1];
+  out[2] = c[2];
+  out[3] = c[3];
+}
+
+/* Batched Philox for tests: out[n][4] for counters ctr[n][4] under one key. */
+void oracle_philox4x32_10_many(const uint32_t* ctr, int64_t n, const uint32_t key[2],
+                               uint32_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) oracle_philox4x32_10(ctr + 4 * i, key, out + 4 * i);
+}
+
+/* The uniforms the method consumes.  r[b][i] (ratio test at position i) and
+ * s[b][j] (resample or bonus draw at position j) for j = 0..k, all in (0, 1):
+ * (word + 0.5) * 2^-32 of Philox4x32-10 at counter (position, b, 0, 0). */
+void oracle_uniforms(uint64_t seed, int B, int k, double* r, double* s) {
+  const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  for (int b = 0; b < B; ++b) {
+    for (int pos = 0; pos <= k; ++pos) {
+      const uint32_t ctr[4] = {(uint32_t)pos, (uint32_t)b, 0u, 0u};
+      uint32_t w[4];
+      oracle_philox4x32_10(ctr, key, w);
+      if (pos < k) r[(size_t)b * k + pos] = ((double)w[0] + 0.5) * 0x1p-32;
+      s[(size_t)b * (k + 1) + pos] = ((double)w[1] + 0.5) * 0x1p-32;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------------
+ * Modified rejection sampling with the uniforms given explicitly.
+ *
+ * p: [B, k+1, V] target probabilities (row i scores position i; row k is the bonus
+ *    row); q: [B, k, V] draft probabilities; draft: [B, k] proposed tokens.
+ * r: [B, k] and s: [B, k+1] uniforms in (0, 1).
+ *
+ * For each sequence, following the neuralmasteryai page's four steps and the
+ * syslabs.in loop:
+ *   for i = 0 .. k-1: accept x_i iff r_i <= min(1, p_i(x_i) / q_i(x_i)), tested as
+ *                     r_i * q_i(x_i) <= p_i(x_i); stop at the first rejection j.
+ *   if a rejection happened at j: draw from max(0, p_j - q_j) / sum (residual);
+ *   otherwise (j = k):            draw the bonus token from p_k.
+ *   The draw emits the smallest x with sum_{y<=x} w(y) > s_j * sum_y w(y).
+ * Outputs: accepted_len[b] = j; out_tokens[b] = x_0..x_{j-1}, drawn, then -1.
+ *
+ * margin[b] (optional) is the smallest distance, in uniform space, between a
+ * uniform that decided this sequence's outcome and the threshold it was compared
+ * with; flag_pos[b] (optional) is the first position whose decision lay within
+ * `flag_window` of its threshold, or -1.
+ * fallback[b] (optional) is 1 when a zero residual forced the draw from p_j.
+ * Returns ORC_OK, ORC_E_TOKEN for a draft outside [0, V), ORC_E_DIST when the row
+ * to draw from has no positive weight (that sequence then emits -1 at position j).
+ * ---------------------------------------------------------------------------- */
+/* One sequence of the rule above; w is a scratch row of V doubles. */
+static int verify_one(const float* pb, const float* qb, const int32_t* xb, const double* rb,
+                      const double* sb, int k, int V, double flag_window, double* w,
+                      int32_t* acc_out, int32_t* ob, double* margin_out, int32_t* flag_out,
+                      int32_t* fallback_out) {
+  for (int t = 0; t <= k; ++t) ob[t] = -1;
+  double mg = INFINITY;
+  int first_flag = -1;
+  int used_fallback = 0;
+  for (int i = 0; i < k; ++i) {
+    if (xb[i] < 0 || xb[i] >= V) {
+      *acc_out = -1;
+      *margin_out = 0.0;
+      *flag_out = -1;
+      *fallback_out = 0;
+      return ORC_E_TOKEN;
+    }
+  }
+
+  /* 1. Ratio tests, left to right, halting at the first rejection. */
+  int j = k;
+  for (int i = 0; i < k; ++i) {
+    const int x = xb[i];
+    const double pi = (double)pb[(size_t)i * V + x];
+    const double qi = (double)qb[(size_t)i * V + x];
+    const double ri = rb[i];
+    if (qi > 0.0) {
+      const double d = fabs(ri - pi / qi);
+      if (d < mg) mg = d;
+      if (d < flag_window && first_flag < 0) first_flag = i;
+    }
+    if (ri * qi <= pi) {
+      ob[i] = x; /* accepted */
+    } else {
+      j = i; /* rejected: halt */
+      break;
+    }
+  }
+
+  /* 2. The row to draw from: residual max(0, p_j - q_j) or the bonus row p_k. */
+  double S = 0.0;
+  for (int x = 0; x < V; ++x) {
+    if (j < k) {
+      const double diff = (double)pb[(size_t)j * V + x] - (double)qb[(size_t)j * V + x];
+      w[x] = diff > 0.0 ? diff : 0.0;
+    } else {
+      w[x] = (double)pb[(size_t)k * V + x];
+    }
+    S += w[x];
+  }
+  if (S == 0.0 && j < k) {
+    /* Zero residual after a rejection: draw from p_j instead. */
+    used_fallback = 1;
+    for (int x = 0; x < V; ++x) {
+      w[x] = (double)pb[(size_t)j * V + x];
+      S += w[x];
+    }
+  }
+
+  /* 3. Inverse-CDF draw: smallest x with prefix(x) > s_j * S. */
+  int status = ORC_OK;
+  const double sj = sb[j];
+  const double target = sj * S;
+  int drawn = -1;
+  if (S > 0.0) {
+    double c = 0.0;
+    for (int x = 0; x < V; ++x) {
+      const double before = c;
+      c += w[x];
+      if (w[x] > 0.0 && c > target) {
+        drawn = x;
+        const double d = fmin(sj - before / S, c / S - sj);
+        if (d < mg) mg = d;
+        if (d < flag_window && first_flag < 0) first_flag = j;
+        break;
+      }
+    }
+    if (drawn < 0) {
+      /* Rounding left the target at or beyond the total: last token with mass. */
+      for (int x = V - 1; x >= 0; --x)
+        if (w[x] > 0.0) {
+          drawn = x;
+          break;
+        }
+      mg = 0.0;
+      if (first_flag < 0) first_flag = j;
+    }
+  } else {
+    status = ORC_E_DIST;
+  }
+  ob[j] = drawn;
+  *acc_out = j;
+  *margin_out = mg;
+  *flag_out = first_flag;
+  *fallback_out = used_fallback;
+  return status;
+}
+
+int oracle_spec_verify_given_uniforms(const float* p, const float* q, const int32_t* draft,
+                                      const double* r, const double* s, int B, int k, int V,
+                                      double flag_window, int32_t* accepted_len,
+                                      int32_t* out_tokens, double* margin, int32_t* flag_pos,
+                                      int32_t* fallback) {
+  if (B < 0 || k < 0 || V <= 0) return ORC_E_ARG;
+  int worst = ORC_OK;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    int local = w ? ORC_OK : ORC_E_ARG;
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+      if (!w) continue;
+      double mg;
+      int32_t fp, fb;
+      const int rc = verify_one(p + (size_t)b * (k + 1) * V, q + (size_t)b * k * V,
+                                draft + (size_t)b * k, r + (size_t)b * k,
+                                s + (size_t)b * (k + 1), k, V, flag_window, w,
+                                accepted_len + b, out_tokens + (size_t)b * (k + 1), &mg, &fp,
+                                &fb);
+      if (margin) margin[b] = mg;
+      if (flag_pos) flag_pos[b] = fp;
+      if (fallback) fallback[b] = fb;
+      if (rc != ORC_OK && local == ORC_OK) local = rc;
+    }
+    free(w);
+#pragma omp critical
+    {
+      if (local != ORC_OK && (worst == ORC_OK || local < worst)) worst = local;
+    }
+  }
+  return worst;
+}
+
+/* Full oracle: Philox uniforms followed by the rejection rule above. */
+int oracle_spec_verify(const float* p, const float* q, const int32_t* draft, uint64_t seed,
+                       int B, int k, int V, double flag_window, int32_t* accepted_len,
+                       int32_t* out_tokens, double* margin, int32_t* flag_pos,
+                       int32_t* fallback) {
+  if (B < 0 || k < 0 || V <= 0) return ORC_E_ARG;
+  double* r = (double*)malloc(sizeof(double) * ((size_t)B * k + 1));
+  double* s = (double*)malloc(sizeof(double) * ((size_t)B * (k + 1) + 1));
+  if (!r || !s) {
+    free(r);
+    free(s);
+    return ORC_E_ARG;
+  }
+  oracle_uniforms(seed, B, k, r, s);
+  const int rc = oracle_spec_verify_given_uniforms(p, q, draft, r, s, B, k, V, flag_window,
+                                                   accepted_len, out_tokens, margin, flag_pos,
+                                                   fallback);
+  free(r);
+  free(s);
+  return rc;
+}
