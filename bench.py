@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Benchmark of the hot path of one continuous-batching iteration on GB300.
+
+A step is one pass of the whole path over one batch: paged decode/verify attention
+(plan + split-KV attention + LSE merge) followed by spec_verify for the batch's verify
+sequences.  Default workload: the 70B-shape stress batch (512 sequences, 64/8 heads,
+d=128, bf16, page 32; 448 decode + 64 verify with k=4; vocab 128256).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is algorithmic bytes per step / device time per
+step (GB/s) with every input resident in HBM; `e2e` is the same metric through the C ABI
+with the step's inputs copied from pinned host memory and its results read back inside
+the timed region (the KV page pool is the cache itself and stays resident).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn achieved HBM GB/s (% of GB300 peak); spec-verify seqs/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stress70b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------------
+# Algorithmic bytes (each KV element read once per KV head, Q in, out + lse out, the
+# block-table entries used; spec_verify: the row(s) it must read plus scalars).
+# ---------------------------------------------------------------------------------
+def attn_bytes(seq_lens, query_lens, Hq, Hkv, D, P, elem):
+    L = np.asarray(seq_lens, dtype=np.int64)
+    ql = np.asarray(query_lens, dtype=np.int64)
+    kv = int((L * Hkv * D * 2 * elem).sum())
+    qo = int((ql * Hq * D * 2 * elem).sum())
+    bt = int(((L + P - 1) // P * 4).sum())
+    lse = int((ql * Hq * 4).sum())
+    return kv + qo + bt + lse
+
+
+def verify_bytes(accepted_len, k, V):
+    acc = np.asarray(accepted_len)
+    rows = np.where(acc < k, 2, 1)  # residual needs p_j and q_j; the bonus needs p_k
+    scalars = k * 4 + k * 8 + (k + 1) * 4 + 4
+    return int((rows * V * 4).sum() + len(acc) * scalars)
+
+
+def workload_desc(name):
+    from verify_attention_spec_gb300 import workloads as wl
+    w = wl.WORKLOADS[name]
+    return (f"{name}: {w.num_seqs} seqs ({w.num_seqs - w.num_verify} decode + {w.num_verify} "
+            f"verify k={w.k}), Hq/Hkv {w.num_q_heads}/{w.num_kv_heads}, d {w.head_dim}, "
+            f"{w.kv_dtype}, page {w.page_size}, lengths {w.length_law}{w.length_args or w.fixed_lens}; "
+            f"spec_verify vocab {w.vocab}")
+
+
+# ---------------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# ncu evidence (committed summary): DRAM traffic per launch of the attention kernel,
+# valid only while the kernel source is unchanged.
+# ---------------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ["paged_attn.cu", "device_util.cuh"]:
+        with open(os.path.join(ROOT, "verify_attention_spec_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    path = os.path.join(ROOT, "profiles", f"paged_attn_{workload}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+# ---------------------------------------------------------------------------------
+# The oracle on the host cores (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------------
+def oracle_sample(a, seqs):
+    """Host copy of the chosen sequences with a compact pool (oracle input)."""
+    import torch
+    from verify_attention_spec_gb300 import workloads as wl
+    bt = a.block_table.cpu().numpy()
+    lens = a.seq_lens.cpu().numpy()
+    qlens = a.query_lens.cpu().numpy()
+    row0 = np.concatenate([[0], np.cumsum(qlens)])
+    P = a.page_size
+    ids, rows, nbt = [], [], []
+    for i in seqs:
+        n = (lens[i] + P - 1) // P
+        base = sum(len(x) for x in ids)
+        ids.append(bt[i, :n])
+        nbt.append(np.arange(base, base + n, dtype=np.int32))
+        rows.append(np.arange(row0[i], row0[i + 1]))
+    idx = torch.from_numpy(np.concatenate(ids).astype(np.int64)).to(a.k_pages.device)
+    maxp = max(len(x) for x in nbt)
+    btn = np.full((len(seqs), maxp), -1, dtype=np.int32)
+    for r, x in enumerate(nbt):
+        btn[r, :len(x)] = x
+    r = torch.from_numpy(np.concatenate(rows)).to(a.q.device)
+    st = lambda t: wl.storage_for_oracle(t, a.kv_dtype)
+    return dict(q=st(a.q[r]), k=st(a.k_pages[idx]), v=st(a.v_pages[idx]), bt=btn,
+                lens=lens[seqs], qlens=qlens[seqs])
+
+
+def time_oracle_attention(sample, kv_dtype):
+    import oracle
+    from verify_attention_spec_gb300 import workloads as wl
+    code = oracle.BF16 if kv_dtype == wl.BF16 else oracle.F32
+    t0 = time.perf_counter()
+    oracle.paged_attn(sample["q"], sample["k"], sample["v"], sample["bt"], sample["lens"],
+                      sample["qlens"], dtype_code=code)
+    return time.perf_counter() - t0
+
+
+def choose_oracle_sample(a, target_s, rng_seed=0):
+    """Grow a seeded random sample of sequences (doubling) until the oracle takes at
+    least target_s seconds on it, or the batch is exhausted."""
+    order = np.random.default_rng(rng_seed).permutation(a.num_seqs)
+    n = 4
+    while True:
+        seqs = sorted(order[:n].tolist())
+        smp = oracle_sample(a, seqs)
+        dt = time_oracle_attention(smp, a.kv_dtype)
+        if dt >= target_s or n >= a.num_seqs:
+            return seqs, smp, dt
+        n = min(a.num_seqs, max(n * 2, int(n * target_s / max(dt, 1e-3) * 1.1)))
+
+
+def cpu_baseline(a, v, name):
+    import oracle
+    w = a
+    seqs, smp, dt = choose_oracle_sample(a, 10.0)
+    by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                    w.page_size, 2 if w.kv_dtype == "bf16" else 4)
+    out = {"value": by / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"paged attention on {len(seqs)} of {a.num_seqs} sequences of {name} "
+                     f"({by / 1e9:.3f} GB algorithmic, {dt:.1f} s)"}
+    if v is not None:
+        t0 = time.perf_counter()
+        oracle.spec_verify(v.p, v.q, v.draft, v.seed)
+        tv = time.perf_counter() - t0
+        out["spec_verify_seqs_per_s"] = v.B / tv
+        out["sample"] += f"; spec_verify on all {v.B} verify sequences ({tv:.2f} s)"
+    return out
+
+
+# ---------------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    from verify_attention_spec_gb300 import binding as vas
+    from verify_attention_spec_gb300 import workloads as wl
+
+    name = args.workload
+    w = wl.WORKLOADS[name]
+    a = wl.workload_attention(name, pool_device=dev)
+    a = wl.AttentionInputs(*(t.to(dev).contiguous() for t in (a.q, a.k_pages, a.v_pages,
+                                                               a.block_table, a.seq_lens,
+                                                               a.query_lens)),
+                           a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
+    v = wl.workload_verify(name)
+    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
+    ws = vas.alloc_workspace(dims, device=dev)
+    out = torch.empty_like(a.q)
+    lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=dev)
+    if v is not None:
+        p_d = torch.from_numpy(v.p).to(dev)
+        q_d = torch.from_numpy(v.q).to(dev)
+        x_d = torch.from_numpy(v.draft).to(dev)
+        acc_d = torch.empty(v.B, dtype=torch.int32, device=dev)
+        tok_d = torch.empty(v.B, v.k + 1, dtype=torch.int32, device=dev)
+
+    def step():
+        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
+                           out, lse, ws, dims=dims)
+        if v is not None:
+            vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
+
+    elem = 2 if a.kv_dtype == wl.BF16 else 4
+    a_bytes = attn_bytes(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
+                         a.num_kv_heads, a.head_dim, a.page_size, elem)
+    step()
+    torch.cuda.synchronize()
+    v_bytes = verify_bytes(acc_d.cpu().numpy(), v.k, v.V) if v is not None else 0
+    step_bytes = a_bytes + v_bytes
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record()
+    for i in range(K):
+        ev[i][0].record()
+        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
+                           out, lse, ws, dims=dims)
+        ev[i][1].record()
+        if v is not None:
+            vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
+        ev[i][2].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    ver_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev])) if v is not None else 0.0
+    ms_per_step = total_ms / K
+    launches_per_step = 3 + (1 if v is not None else 0)
+
+    # e2e: the same step through the C ABI from pinned host buffers.
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.cpu().pin_memory() for t in (a.q, a.block_table, a.seq_lens, a.query_lens)]
+        dev_in = [torch.empty_like(t) for t in (a.q, a.block_table, a.seq_lens, a.query_lens)]
+        if v is not None:
+            host_v = [torch.from_numpy(x).pin_memory() for x in (v.p, v.q, v.draft)]
+            dev_v = [torch.empty_like(t, device=dev) for t in host_v]
+        host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                    torch.empty(lse.shape, dtype=lse.dtype).pin_memory()]
+        if v is not None:
+            host_out += [torch.empty(acc_d.shape, dtype=torch.int32).pin_memory(),
+                         torch.empty(tok_d.shape, dtype=torch.int32).pin_memory()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in + (host_v if v is not None else []))
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            for hsrc, dd in zip(host_in, dev_in):
+                dd.copy_(hsrc, non_blocking=True)
+            vas.paged_attn_fwd(dev_in[0], a.k_pages, a.v_pages, dev_in[1], dev_in[2], dev_in[3],
+                               out, lse, ws, dims=dims)
+            if v is not None:
+                for hsrc, dd in zip(host_v, dev_v):
+                    dd.copy_(hsrc, non_blocking=True)
+                vas.spec_verify(dev_v[0], dev_v[1], dev_v[2], v.seed, acc_d, tok_d)
+            host_out[0].copy_(out, non_blocking=True)
+            host_out[1].copy_(lse, non_blocking=True)
+            if v is not None:
+                host_out[2].copy_(acc_d, non_blocking=True)
+                host_out[3].copy_(tok_d, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
+        e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+
+    peak, peak_src = measured_peak()
+    attn_gbs = a_bytes / (attn_ms * 1e-3) / 1e9
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if a.kv_dtype == wl.BF16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(name),
+                   "l2": "inputs larger than L2 (KV pool %.1f GB per step)"
+                         % ((a.k_pages.numel() + a.v_pages.numel()) * elem / 1e9),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "paged_attn": {"gbs": attn_gbs, "ms": attn_ms, "algorithmic_bytes": a_bytes,
+                       "frac_of_measured_peak": attn_gbs / peak,
+                       "frac_of_nominal_8tbs": attn_gbs / NOMINAL_HBM_GBS},
+        "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": attn_gbs / peak, "traffic": ncu_traffic(name),
+                     "peak_source": peak_src,
+                     "kernel": "paged_attn_fwd (plan + attention + LSE merge)"},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if v is not None:
+        acc = acc_d.cpu().numpy()
+        res["spec_verify"] = {"seqs_per_s": v.B / (ver_ms * 1e-3), "ms": ver_ms,
+                              "gbs": v_bytes / (ver_ms * 1e-3) / 1e9, "algorithmic_bytes": v_bytes,
+                              "mean_accepted": float(acc.mean()),
+                              "acceptance_rate": float(acc.mean() / v.k)}
+    if e2e is not None:
+        res["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(a, v, name)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------
+# Reference arm: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from verify_attention_spec_gb300 import workloads as wl
+    name = args.workload
+    w = wl.WORKLOADS[name]
+    # the inputs: the same workload, its pool drawn on the host (no GPU on this leg)
+    lens, qlens = wl.sample_lengths(w), wl.query_lengths(w)
+    order = np.random.default_rng(0).permutation(len(lens))
+    # a bounded sample: sequences in seeded order up to ~64 MB of KV
+    elem = 2 if w.kv_dtype == wl.BF16 else 4
+    per_tok = w.num_kv_heads * w.head_dim * 2 * elem
+    seqs, tot = [], 0
+    for i in order:
+        if seqs and tot + lens[i] * per_tok > 64e6:
+            break
+        seqs.append(int(i))
+        tot += lens[i] * per_tok
+    seqs.sort()
+    a = wl.attention_inputs(lens[seqs], qlens[seqs], num_q_heads=w.num_q_heads,
+                            num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                            page_size=w.page_size, kv_dtype=w.kv_dtype, seed=w.seed)
+    v = wl.workload_verify(name)
+    code = oracle.BF16 if w.kv_dtype == wl.BF16 else oracle.F32
+    st = lambda t: wl.storage_for_oracle(t, w.kv_dtype)
+    smp = dict(q=st(a.q), k=st(a.k_pages), v=st(a.v_pages), bt=a.block_table.numpy(),
+               lens=a.seq_lens.numpy(), qlens=a.query_lens.numpy())
+    by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
+                    w.page_size, elem)
+
+    def step():
+        oracle.paged_attn(smp["q"], smp["k"], smp["v"], smp["bt"], smp["lens"], smp["qlens"],
+                          dtype_code=code)
+        if v is not None:
+            oracle.spec_verify(v.p[:8], v.q[:8], v.draft[:8], v.seed)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    vb = verify_bytes(np.zeros(8, np.int32), v.k, v.V) if v is not None else 0
+    value = (by + vb) / dt / 1e9
+    sample = (f"per step: paged attention on {len(seqs)} of {w.num_seqs} sequences of {name} "
+              f"({by / 1e9:.3f} GB algorithmic)" + (f" + spec_verify on 8 of {v.B} verify sequences"
+                                                    if v is not None else ""))
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": workload_desc(name)},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

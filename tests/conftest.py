@@ -25,3 +25,12 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def vas_lib():
+    """Build libvas.so if it is missing or stale, then import the binding."""
+    from verify_attention_spec_gb300 import _build
+    _build.build()
+    from verify_attention_spec_gb300 import binding
+    return binding

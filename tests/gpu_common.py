@@ -1,0 +1,106 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI and the
+oracle on the same seeded inputs, and compare with the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from verify_attention_spec_gb300 import workloads as wl
+
+# Attention tolerances (output vs the float64 oracle): max-abs 1e-2 and relative L2 5e-3
+# for bf16 storage, 1e-5 for fp32 storage.  lse is fp32 in both cases; its error is that
+# of an fp32 dot product of length D (bf16 inputs are exact), so 2e-3 / 2e-5 absolute.
+TOL = {wl.BF16: dict(max_abs=1e-2, rel_l2=5e-3, lse=2e-3),
+       wl.F32: dict(max_abs=1e-5, rel_l2=1e-5, lse=2e-5)}
+
+
+def to_device(a: wl.AttentionInputs, device="cuda") -> wl.AttentionInputs:
+    mv = lambda t: t.to(device, non_blocking=False).contiguous()
+    return wl.AttentionInputs(mv(a.q), mv(a.k_pages), mv(a.v_pages), mv(a.block_table),
+                              mv(a.seq_lens), mv(a.query_lens), a.num_q_heads, a.num_kv_heads,
+                              a.head_dim, a.page_size, a.kv_dtype)
+
+
+def run_gpu_attention(vas, a: wl.AttentionInputs, workspace_bytes=None, out=None, lse=None):
+    d = a.q.device
+    if out is None:
+        out = torch.empty_like(a.q)
+    if lse is None:
+        lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=d)
+    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
+    ws = vas.alloc_workspace(dims, device=d, nbytes=workspace_bytes)
+    vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens, out,
+                       lse, ws, dims=dims)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_attention(a: wl.AttentionInputs):
+    code = oracle.BF16 if a.kv_dtype == wl.BF16 else oracle.F32
+    st = lambda t: wl.storage_for_oracle(t, a.kv_dtype)
+    return oracle.paged_attn(st(a.q), st(a.k_pages), st(a.v_pages), a.block_table.cpu().numpy(),
+                             a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), dtype_code=code)
+
+
+def compare_attention(out, lse, ref_out, ref_lse, kv_dtype, rows=None):
+    tol = TOL[kv_dtype]
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        o, l = o[rows], l[rows]
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+    err = np.abs(o - ref_out)
+    max_abs = float(err.max()) if err.size else 0.0
+    rel_l2 = float(np.linalg.norm(o - ref_out) / max(np.linalg.norm(ref_out), 1e-30))
+    lse_err = float(np.abs(l - ref_lse).max()) if l.size else 0.0
+    assert max_abs <= tol["max_abs"], f"max-abs {max_abs}"
+    assert rel_l2 <= tol["rel_l2"], f"rel-L2 {rel_l2}"
+    assert lse_err <= tol["lse"], f"lse {lse_err}"
+    return dict(max_abs=max_abs, rel_l2=rel_l2, lse=lse_err)
+
+
+def subset_inputs(a: wl.AttentionInputs, seqs) -> wl.AttentionInputs:
+    """The chosen sequences only, with their pages copied into a compact pool (the block
+    table is renumbered; paging is invisible to the result).  CPU tensors."""
+    bt = a.block_table.cpu().numpy()
+    lens = a.seq_lens.cpu().numpy()
+    qlens = a.query_lens.cpu().numpy()
+    row0 = np.concatenate([[0], np.cumsum(qlens)])
+    P = a.page_size
+    pages, new_bt, q_rows = [], [], []
+    for i in seqs:
+        n = (lens[i] + P - 1) // P
+        ids = bt[i, :n]
+        base = sum(len(p) for p in pages)
+        pages.append(ids)
+        new_bt.append(np.arange(base, base + n, dtype=np.int32))
+        q_rows.append(np.arange(row0[i], row0[i + 1]))
+    all_ids = torch.from_numpy(np.concatenate(pages).astype(np.int64)).to(a.k_pages.device)
+    maxp = max(len(r) for r in new_bt)
+    btn = np.full((len(seqs), maxp), -1, dtype=np.int32)
+    for r, ids in enumerate(new_bt):
+        btn[r, :len(ids)] = ids
+    rows = torch.from_numpy(np.concatenate(q_rows)).to(a.q.device)
+    return wl.AttentionInputs(a.q[rows].cpu(), a.k_pages[all_ids].cpu(), a.v_pages[all_ids].cpu(),
+                              torch.from_numpy(btn), torch.from_numpy(lens[seqs].astype(np.int32)),
+                              torch.from_numpy(qlens[seqs].astype(np.int32)), a.num_q_heads,
+                              a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype), np.concatenate(q_rows)
+
+
+def compare_verify(acc, out, ref):
+    """Bit-exact except sequences the oracle flags (a uniform within the window of its
+    threshold): those must agree before the flagged position.  Returns flagged count."""
+    acc = np.asarray(acc)
+    out = np.asarray(out)
+    flagged = 0
+    for b in range(len(acc)):
+        f = int(ref.flag_pos[b])
+        if f < 0:
+            assert acc[b] == ref.accepted_len[b], (b, acc[b], ref.accepted_len[b])
+            np.testing.assert_array_equal(out[b], ref.out_tokens[b], err_msg=f"sequence {b}")
+        else:
+            flagged += 1
+            np.testing.assert_array_equal(out[b, :f], ref.out_tokens[b, :f])
+            assert acc[b] >= min(f, ref.accepted_len[b])
+    return flagged

@@ -1,0 +1,96 @@
+"""The C-ABI library loads, exports every entry point include/vas.h declares, and
+rejects bad arguments on the host (no kernel is launched by these checks)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "vas.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\([^;{]*\)\s*;", text)
+    return sorted(set(n for n in names if n not in ("if", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["paged_attn_fwd", "paged_attn_workspace_size", "spec_verify", "vas_last_device_error",
+              "vas_pool_create", "vas_build_block_table", "vas_seq_rollback"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(vas_lib):
+    lib = ctypes.CDLL(vas_lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _dims(vas_lib, **kw):
+    d = dict(num_seqs=4, total_q_tokens=10, num_q_heads=32, num_kv_heads=8, head_dim=128,
+             page_size=16, num_pages=100, max_pages_per_seq=10, kv_dtype=vas_lib.VAS_BF16, scale=0.0)
+    d.update(kw)
+    return vas_lib.vas_attn_dims(**d)
+
+
+def test_workspace_queries(vas_lib):
+    d = _dims(vas_lib)
+    mn, rec = vas_lib.paged_attn_workspace_min(d), vas_lib.paged_attn_workspace_size(d)
+    assert 0 < mn <= rec
+    # partial capacity grows with the output rows
+    d2 = _dims(vas_lib, total_q_tokens=1000)
+    assert vas_lib.paged_attn_workspace_size(d2) > rec
+    for bad in [dict(num_q_heads=30), dict(head_dim=96), dict(page_size=8), dict(kv_dtype=7),
+                dict(num_seqs=-1)]:
+        assert vas_lib.paged_attn_workspace_size(_dims(vas_lib, **bad)) == 0
+
+
+def test_host_validation_without_launch(vas_lib):
+    lib = vas_lib._lib
+    P = ctypes.c_void_p
+    fake = P(1 << 20)  # never dereferenced: validation fails first
+    d = _dims(vas_lib)
+    null = P(0)
+    st = lib.paged_attn_fwd(null, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(d), fake,
+                            1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG
+    st = lib.paged_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake,
+                            ctypes.byref(_dims(vas_lib, head_dim=80)), fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_UNSUPPORTED
+    st = lib.paged_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake,
+                            ctypes.byref(_dims(vas_lib, num_q_heads=33)), fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG
+    misaligned = P((1 << 20) + 8)
+    st = lib.paged_attn_fwd(misaligned, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(d),
+                            fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG
+    st = lib.paged_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(d), fake,
+                            16, null)
+    assert st == vas_lib.VAS_E_WORKSPACE
+    # empty batch is a no-op
+    assert lib.paged_attn_fwd(null, null, null, null, null, null, null, null,
+                              ctypes.byref(_dims(vas_lib, num_seqs=0)), null, 0, null) == vas_lib.VAS_OK
+    # spec_verify argument checks
+    assert lib.spec_verify(fake, fake, fake, 1, fake, fake, 4, 3, 0, null) == vas_lib.VAS_E_INVALID_ARG
+    assert lib.spec_verify(null, fake, fake, 1, fake, fake, 4, 3, 10, null) == vas_lib.VAS_E_INVALID_ARG
+    assert lib.spec_verify(fake, fake, fake, 1, fake, fake, -1, 3, 10, null) == vas_lib.VAS_E_INVALID_ARG
+    assert lib.spec_verify(fake, null, null, 1, fake, fake, 4, 3, 10, null) == vas_lib.VAS_E_INVALID_ARG
+    assert lib.spec_verify(null, null, null, 1, null, null, 0, 3, 10, null) == vas_lib.VAS_OK
+    assert lib.vas_status_string(vas_lib.VAS_E_WORKSPACE) == b"workspace too small"
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    """The product package raises when libvas.so is absent instead of falling back."""
+    import subprocess
+    import sys
+    pkg = tmp_path / "verify_attention_spec_gb300"
+    pkg.mkdir()
+    src = os.path.join(ROOT, "verify_attention_spec_gb300")
+    for f in ["__init__.py", "binding.py", "workloads.py"]:
+        (pkg / f).write_text(open(os.path.join(src, f)).read())
+    code = "import verify_attention_spec_gb300.binding"
+    res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
+    assert res.returncode != 0 and "libvas.so" in res.stderr and "ImportError" in res.stderr

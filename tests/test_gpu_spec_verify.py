@@ -1,0 +1,144 @@
+"""GPU parity of spec_verify (modified rejection sampling) against the oracle, through the
+C ABI (include/vas.h: spec_verify).  Accepted lengths and tokens are bit-exact except for
+sequences where a uniform lies within 1e-6 of its threshold (flagged by the oracle)."""
+import numpy as np
+import pytest
+import torch
+from scipy.stats import chisquare
+
+import oracle
+from verify_attention_spec_gb300 import workloads as wl
+
+from gpu_common import compare_verify
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu_verify(vas, p, q, draft, seed):
+    B, k1, V = p.shape
+    pd = torch.from_numpy(np.ascontiguousarray(p)).cuda()
+    qd = torch.from_numpy(np.ascontiguousarray(q)).cuda()
+    xd = torch.from_numpy(np.ascontiguousarray(draft, dtype=np.int32)).cuda()
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((B, k1), -7, dtype=torch.int32, device="cuda")
+    vas.spec_verify(pd, qd, xd, seed, acc, out)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), out.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "verify32", "mixed272", "stress70b"])
+def test_workload_parity(vas_lib, name):
+    v = wl.workload_verify(name)
+    ref = oracle.spec_verify(v.p, v.q, v.draft, v.seed)
+    assert ref.status == oracle.OK
+    acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, v.seed)
+    flagged = compare_verify(acc, out, ref)
+    assert flagged <= max(1, v.B // 20)
+    assert vas_lib.vas_last_device_error() == 0
+
+
+@pytest.mark.parametrize("V", [1, 7, 1001, 5000])
+def test_odd_vocab_and_many_sequences(vas_lib, V):
+    """Vocabularies that are not a multiple of four take the scalar load path."""
+    v = wl.verify_inputs(300, 3, V, seed=V, p_logit_std=2.0, q_noise_std=1.0)
+    ref = oracle.spec_verify(v.p, v.q, v.draft, 77)
+    acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, 77)
+    compare_verify(acc, out, ref)
+
+
+def test_k0_plain_sampling_and_seed_changes(vas_lib):
+    v = wl.verify_inputs(500, 0, 64, seed=2)
+    for seed in (0, 1, 2**63 + 5):
+        ref = oracle.spec_verify(v.p, v.q, v.draft, seed)
+        acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, seed)
+        compare_verify(acc, out, ref)
+        assert np.all(acc == 0)
+
+
+def test_chi_square_million_draws(vas_lib):
+    """10^6 GPU draws: the first emitted token follows p_0 (the pages' lossless claim) and
+    the bonus token after full acceptance follows p_k (chi-square, p > 0.01)."""
+    rng = np.random.default_rng(31)
+    B, k, V = 1_000_000, 2, 16
+    logits = rng.normal(0, 1.0, size=(k + 1, V))
+    p1 = np.exp(logits) / np.exp(logits).sum(-1, keepdims=True)
+    qq = np.exp(logits[:k] + rng.normal(0, 0.8, size=(k, V)))
+    q1 = qq / qq.sum(-1, keepdims=True)
+    p32, q32 = p1.astype(np.float32), q1.astype(np.float32)
+    x = np.stack([rng.choice(V, size=B, p=q1[i]) for i in range(k)], axis=1).astype(np.int32)
+    pd = torch.from_numpy(p32).cuda().expand(B, k + 1, V).contiguous()
+    qd = torch.from_numpy(q32).cuda().expand(B, k, V).contiguous()
+    xd = torch.from_numpy(x).cuda()
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, k + 1, dtype=torch.int32, device="cuda")
+    vas_lib.spec_verify(pd, qd, xd, 20261202, acc, out)
+    torch.cuda.synchronize()
+    acc, out = acc.cpu().numpy(), out.cpu().numpy()
+    p0 = p32[0].astype(np.float64)
+    f0 = np.bincount(out[:, 0], minlength=V)
+    assert chisquare(f0, B * p0 / p0.sum()).pvalue > 0.01
+    full = acc == k
+    pk = p32[k].astype(np.float64)
+    fk = np.bincount(out[full, k], minlength=V)
+    assert chisquare(fk, full.sum() * pk / pk.sum()).pvalue > 0.01
+
+
+def test_equal_and_disjoint_and_greedy(vas_lib):
+    rng = np.random.default_rng(4)
+    B, k, V = 64, 4, 40
+    p = rng.dirichlet(np.ones(V), size=(B, k + 1)).astype(np.float32)
+    x = rng.integers(0, V, size=(B, k)).astype(np.int32)
+    acc, out = run_gpu_verify(vas_lib, p, p[:, :k].copy(), x, 9)
+    assert np.all(acc == k) and np.all(out[:, :k] == x)
+    # disjoint supports
+    pd = np.zeros((B, k + 1, V), np.float32)
+    qd = np.zeros((B, k, V), np.float32)
+    pd[:, :, :20] = 1 / 20
+    qd[:, :, 20:] = 1 / 20
+    xd = np.full((B, k), 25, np.int32)
+    acc, out = run_gpu_verify(vas_lib, pd, qd, xd, 9)
+    assert np.all(acc == 0) and np.all(out[:, 0] < 20) and np.all(out[:, 1:] == -1)
+    # one-hot rows: greedy exact matching
+    tgt = rng.integers(0, V, size=(B, k + 1))
+    drf = np.where(rng.random((B, k)) < 0.6, tgt[:, :k], rng.integers(0, V, size=(B, k))).astype(np.int32)
+    po = np.zeros((B, k + 1, V), np.float32)
+    qo = np.zeros((B, k, V), np.float32)
+    po[np.arange(B)[:, None], np.arange(k + 1)[None], tgt] = 1
+    qo[np.arange(B)[:, None], np.arange(k)[None], drf] = 1
+    ref = oracle.spec_verify(po, qo, drf, 3)
+    acc, out = run_gpu_verify(vas_lib, po, qo, drf, 3)
+    np.testing.assert_array_equal(acc, ref.accepted_len)
+    np.testing.assert_array_equal(out, ref.out_tokens)
+
+
+def test_error_paths(vas_lib):
+    vas_lib.vas_last_device_error()
+    p = np.full((3, 3, 5), 0.2, np.float32)
+    q = np.full((3, 2, 5), 0.2, np.float32)
+    x = np.array([[0, 1], [7, 1], [2, 3]], np.int32)
+    acc, out = run_gpu_verify(vas_lib, p, q, x, 1)
+    assert vas_lib.vas_last_device_error() & vas_lib.VAS_DEV_BAD_TOKEN
+    assert acc[1] == -1 and np.all(out[1] == -1)
+    ref = oracle.spec_verify(p, q, x, 1)
+    assert acc[0] == ref.accepted_len[0] and acc[2] == ref.accepted_len[2]
+    # an empty row to draw from
+    pz = np.zeros((2, 1, 9), np.float32)
+    acc, out = run_gpu_verify(vas_lib, pz, np.zeros((2, 0, 9), np.float32), np.zeros((2, 0), np.int32), 1)
+    assert vas_lib.vas_last_device_error() & vas_lib.VAS_DEV_EMPTY_ROW
+    assert np.all(out[:, 0] == -1) and np.all(acc == 0)
+
+
+def test_zero_residual_fallback_matches_oracle(vas_lib):
+    B, V = 200, 6
+    p = np.zeros((B, 2, V), np.float32)
+    q = np.zeros((B, 1, V), np.float32)
+    p[:, 0, :3] = [0.1, 0.2, 0.1]   # p <= q everywhere: a rejection leaves no residual
+    q[:, 0, :3] = [0.3, 0.4, 0.3]
+    p[:, 1, :] = 1 / V
+    x = np.zeros((B, 1), np.int32)
+    ref = oracle.spec_verify(p, q, x, 12)
+    vas_lib.vas_last_device_error()
+    acc, out = run_gpu_verify(vas_lib, p, q, x, 12)
+    compare_verify(acc, out, ref)
+    if np.any(ref.fallback):
+        assert vas_lib.vas_last_device_error() & vas_lib.VAS_DEV_RESIDUAL_FALLBACK
