@@ -89,8 +89,16 @@ def test_binding_fails_loudly_without_library(tmp_path):
     pkg = tmp_path / "verify_attention_spec_gb300"
     pkg.mkdir()
     src = os.path.join(ROOT, "verify_attention_spec_gb300")
-    for f in ["__init__.py", "binding.py", "workloads.py"]:
+    for f in ["__init__.py", "binding.py", "workloads.py", "_build.py"]:
         (pkg / f).write_text(open(os.path.join(src, f)).read())
-    code = "import verify_attention_spec_gb300.binding"
+    # the build script and the input generators import without the library ...
+    code = ("from verify_attention_spec_gb300 import _build, workloads; "
+            "import verify_attention_spec_gb300 as v; v.workloads.WORKLOADS['tiny']")
     res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True)
-    assert res.returncode != 0 and "libvas.so" in res.stderr and "ImportError" in res.stderr
+    assert res.returncode == 0, res.stderr
+    # ... but the binding (and any compute entry point) refuses to run
+    for code in ["import verify_attention_spec_gb300.binding",
+                 "import verify_attention_spec_gb300 as v; v.paged_attn_fwd"]:
+        res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True,
+                             text=True)
+        assert res.returncode != 0 and "libvas.so" in res.stderr and "ImportError" in res.stderr
