@@ -89,11 +89,12 @@ def subset_inputs(a: wl.AttentionInputs, seqs) -> wl.AttentionInputs:
 
 
 def compare_verify(acc, out, ref):
-    """Bit-exact except sequences the oracle flags (a uniform within the window of its
-    threshold): those must agree before the flagged position.  Returns flagged count."""
+    """Bit-exact except sequences the oracle flags (a uniform within 1e-6 of its
+    threshold): those must agree before the flagged position, and are counted.
+    Returns (flagged, flagged sequences whose outputs differ)."""
     acc = np.asarray(acc)
     out = np.asarray(out)
-    flagged = 0
+    flagged = differ = 0
     for b in range(len(acc)):
         f = int(ref.flag_pos[b])
         if f < 0:
@@ -103,4 +104,6 @@ def compare_verify(acc, out, ref):
             flagged += 1
             np.testing.assert_array_equal(out[b, :f], ref.out_tokens[b, :f])
             assert acc[b] >= min(f, ref.accepted_len[b])
-    return flagged
+            if acc[b] != ref.accepted_len[b] or not np.array_equal(out[b], ref.out_tokens[b]):
+                differ += 1
+    return flagged, differ

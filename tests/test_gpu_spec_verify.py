@@ -32,8 +32,11 @@ def test_workload_parity(vas_lib, name):
     ref = oracle.spec_verify(v.p, v.q, v.draft, v.seed)
     assert ref.status == oracle.OK
     acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, v.seed)
-    flagged = compare_verify(acc, out, ref)
-    assert flagged <= max(1, v.B // 20)
+    flagged, differ = compare_verify(acc, out, ref)
+    print(f"{name}: {v.B} sequences, {flagged} flagged near a boundary, {differ} of them differ")
+    # The GPU's prefix sums sit within ~1e-9 of the oracle's, far inside the 1e-6 window,
+    # so even among flagged sequences a different outcome should be rare.
+    assert differ <= 1
     assert vas_lib.vas_last_device_error() == 0
 
 
