@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--workload", default="stress70b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--max-seqs", type=int, default=0,
+                    help="profiling only: keep the first N sequences of the workload")
     return ap.parse_args()
 
 
@@ -280,12 +282,23 @@ def run_ours(args):
 
     name = args.workload
     w = wl.WORKLOADS[name]
-    a = wl.workload_attention(name, pool_device=dev)
+    if args.max_seqs:
+        lens = wl.sample_lengths(w)[:args.max_seqs]
+        qlens = wl.query_lengths(w)[:args.max_seqs]
+        a = wl.attention_inputs(lens, qlens, num_q_heads=w.num_q_heads,
+                                num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                                page_size=w.page_size, kv_dtype=w.kv_dtype, seed=w.seed,
+                                pool_device=dev)
+    else:
+        a = wl.workload_attention(name, pool_device=dev)
     a = wl.AttentionInputs(*(t.to(dev).contiguous() for t in (a.q, a.k_pages, a.v_pages,
                                                                a.block_table, a.seq_lens,
                                                                a.query_lens)),
                            a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
     v = wl.workload_verify(name)
+    if args.max_seqs and v is not None:
+        nv = max(1, int((qlens > 1).sum()))
+        v = wl.VerifyInputs(v.p[:nv], v.q[:nv], v.draft[:nv], v.seed)
     dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
     ws = vas.alloc_workspace(dims, device=dev)
     out = torch.empty_like(a.q)
@@ -406,7 +419,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16" if a.kv_dtype == wl.BF16 else "f32",
         "data": "synthetic",
-        "config": {"workload": workload_desc(name),
+        "config": {"workload": workload_desc(name) + (f" (first {args.max_seqs} sequences only)"
+                                                       if args.max_seqs else ""),
                    "l2": "inputs larger than L2 (KV pool %.1f GB per step)"
                          % ((a.k_pages.numel() + a.v_pages.numel()) * elem / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
