@@ -353,7 +353,7 @@ def run_ours(args):
     attn_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     ver_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev])) if v is not None else 0.0
     ms_per_step = total_ms / K
-    launches_per_step = 3 + (1 if v is not None else 0)
+    launches_per_step = 2 + (1 if v is not None else 0)  # plan + attention (+ spec_verify)
 
     # e2e: the same step through the C ABI from pinned host buffers.
     e2e = None
@@ -430,7 +430,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
                      "frac": attn_gbs / peak, "traffic": ncu_traffic(name),
                      "peak_source": peak_src,
-                     "kernel": "paged_attn_fwd (plan + attention + LSE merge)"},
+                     "kernel": "paged_attn_fwd (plan + attention with the fused LSE merge)"},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }

@@ -8,22 +8,31 @@
 //
 // How (split-KV, flash-decoding style; the pages give no kernel design):
 //   1. plan_kernel      one CTA: validates lengths, packs query rows, chooses a split
-//                       length in pages and writes the work list (sequence, page range,
-//                       split, row block) to the workspace.
-//   2. attn_bf16_kernel persistent, one CTA per SM.  A producer warp takes work units
-//                       (work item x KV head) from an atomic counter and streams the
-//                       unit's K/V page slices into a 4-stage shared-memory ring with
-//                       TMA (one 3-D box per 128-byte column half of a page), tracked by
-//                       mbarriers.  Four consumer warps run QK^T and PV on the tensor
-//                       cores (mma.sync m16n8k16 bf16 -> fp32) with an online softmax;
-//                       the GQA group x query tokens of one KV head form the MMA rows.
-//                       A unit that covers its whole sequence writes out/lse directly;
-//                       otherwise it writes a normalised fp32 partial and its lse.
-//      attn_f32_kernel  fp32 storage: CUDA-core FMA, one warp per query row.
-//   3. combine_kernel   merges the partials of split sequences by their lse
-//                       (O = sum_s e^{lse_s - m} O_s / sum_s e^{lse_s - m},
-//                       lse = m + ln sum_s e^{lse_s - m}) and NaN-fills rows that a
-//                       device-detected error left undefined.
+//                       length in pages, writes the work list (sequence, page range,
+//                       split, row block), zeroes the split counters and NaN-fills the
+//                       rows of sequences with inconsistent lengths.
+//   2. attn_bf16_kernel persistent, one CTA per SM, launched as a programmatic
+//                       dependent of the plan.  A producer warp takes work units (work
+//                       item x KV head) from an atomic counter and streams the unit's
+//                       K/V page slices into an 8-slot ring of 32-token stages with TMA
+//                       (one 4-D box per page and operand, 128-byte swizzle), tracked by
+//                       mbarriers; it prefetches the next unit's descriptor and block-
+//                       table entries while streaming.  Four consumer warps compute on
+//                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32):
+//                         narrow units (<= 16 query rows per KV head: decode, small
+//                         verify groups) take S^T = K Q^T with the KV tokens as the
+//                         16-row M side and the GQA rows as N, so 8 rows fill an n8 tile;
+//                         P^T reaches the PV operand through movmatrix.  Each warp owns
+//                         whole stages (round robin) and keeps its own online softmax;
+//                         the four are merged at the end of the unit.
+//                         wide units (17..64 rows) take S = Q K^T with the rows as M
+//                         (m16 tiles spread over the warps) and P kept in registers.
+//                       A unit covering its whole sequence writes out/lse; otherwise it
+//                       writes a normalised fp32 partial and its lse, and the last split
+//                       to finish (atomic counter, no waiting) merges them by lse:
+//                       O = sum_s e^{lse_s - m} O_s / sum_s e^{lse_s - m},
+//                       lse = m + ln sum_s e^{lse_s - m}.
+//      attn_f32_kernel  fp32 storage: CUDA-core FMA, one warp per query row, no split.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -34,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/vas.h"
 #include "device_util.cuh"
@@ -42,16 +52,18 @@
 namespace vas {
 namespace attn {
 
-constexpr int kStageTokens = 64;   // KV tokens per pipeline stage
-constexpr int kStages = 4;         // stages in the shared-memory ring
+constexpr int kStageTokens = 32;   // KV tokens per pipeline stage
+constexpr int kSlots = 8;          // stages in the shared-memory ring
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kRowBlock = 64;      // MMA rows per unit (four m16 tiles)
-constexpr int kRing = 4;           // work units the producer may run ahead
+constexpr int kRowBlock = 64;      // query rows per unit (four m16 tiles)
+constexpr int kNarrowRows = 16;    // units with at most this many rows take the K Q^T form
+constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
 constexpr int kUnitsPerSm = 16;    // split target: work units per SM
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemSeqs = 4096;
 constexpr int kSeqInvalid = 1;
 
 struct SeqPlan {
@@ -62,7 +74,7 @@ struct SeqPlan {
   int32_t qlen;          // ql
   int32_t flags;         // kSeqInvalid
   int32_t nrb;           // row blocks
-  int32_t pad;
+  int32_t item0;         // first work item (split 0, row block 0)
 };
 
 struct Item {
@@ -76,8 +88,16 @@ struct PlanHeader {
   int32_t n_partial_rows;
 };
 
+// What the producer hands the consumers for one unit (u < 0: no more work).
+struct RingEntry {
+  int32_t u, head;
+  Item item;
+  SeqPlan sp;
+  int32_t pad[2];
+};
+
 struct Layout {
-  size_t seqplan, token_seq, items, part_lse, part_o, total;
+  size_t seqplan, token_seq, items, counters, part_lse, part_o, total;
   int64_t items_cap, partial_cap;
 };
 
@@ -93,7 +113,10 @@ struct PlanArgs {
   int32_t* token_seq;
   Item* items;
   PlanHeader* header;
-  int32_t B, T, G, Hkv, P, maxp, pps, min_chunk, no_split, target_units;
+  int32_t* counters;
+  void* out;
+  float* lse;
+  int32_t B, T, G, Hkv, Hq, D, P, maxp, pps, min_chunk, no_split, target_units, is_bf16;
   int64_t items_cap, partial_cap;
   int32_t* err;
 };
@@ -110,8 +133,7 @@ __device__ __forceinline__ int64_t block_sum_i64(int64_t v, int64_t* red) {
   return t;
 }
 
-// Exclusive scan of v over the block (threads in order); returns the prefix, stores the
-// block total in *total.
+// Exclusive scan of v over the block (threads in order); *total gets the block total.
 __device__ __forceinline__ int64_t block_excl_scan_i64(int64_t v, int64_t* red,
                                                        int64_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -138,13 +160,13 @@ struct SeqShape {
   int32_t L, ql, npages, R, nrb;
 };
 
-__device__ __forceinline__ SeqShape seq_shape(const PlanArgs& a, int i) {
+__device__ __forceinline__ SeqShape seq_shape(const PlanArgs& a, int32_t L, int32_t ql) {
   SeqShape s;
-  s.L = a.seq_lens[i];
-  s.ql = a.query_lens[i];
-  s.valid = s.ql >= 0 && s.ql <= a.T && s.L >= s.ql && (int64_t)s.L <= (int64_t)a.maxp * a.P;
-  s.npages = s.valid ? (s.L + a.P - 1) / a.P : 0;
-  s.R = s.valid ? a.G * s.ql : 0;
+  s.L = L;
+  s.ql = ql;
+  s.valid = ql >= 0 && ql <= a.T && L >= ql && (int64_t)L <= (int64_t)a.maxp * a.P;
+  s.npages = s.valid ? (L + a.P - 1) / a.P : 0;
+  s.R = s.valid ? a.G * ql : 0;
   s.nrb = (s.R + kRowBlock - 1) / kRowBlock;
   return s;
 }
@@ -155,17 +177,28 @@ __device__ __forceinline__ int32_t splits_for(const SeqShape& s, int64_t chunk) 
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
+  pdl_launch_dependents();  // the attention grid may start its prologue
+  __shared__ int32_t s_L[kPlanSmemSeqs], s_ql[kPlanSmemSeqs];
   __shared__ int64_t red[kPlanThreads / 32];
   __shared__ int64_t s_chunk;
   __shared__ int32_t s_bad;
   const int tid = threadIdx.x;
+  const bool cached = a.B <= kPlanSmemSeqs;
   if (tid == 0) s_bad = 0;
+  if (cached)
+    for (int i = tid; i < a.B; i += kPlanThreads) {
+      s_L[i] = a.seq_lens[i];
+      s_ql[i] = a.query_lens[i];
+    }
   __syncthreads();
+  auto shape = [&](int i) {
+    return cached ? seq_shape(a, s_L[i], s_ql[i]) : seq_shape(a, a.seq_lens[i], a.query_lens[i]);
+  };
 
   // Totals: work in page-row-blocks per KV head, and the packed query rows.
   int64_t cost = 0, rows = 0;
   for (int i = tid; i < a.B; i += kPlanThreads) {
-    const SeqShape s = seq_shape(a, i);
+    const SeqShape s = shape(i);
     if (!s.valid) s_bad = 1;
     cost += (int64_t)s.npages * s.nrb;
     rows += s.ql > 0 ? s.ql : 0;
@@ -177,7 +210,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   // Split length: about kUnitsPerSm units per SM, at least min_chunk pages, a whole
   // number of stages; doubled until the work list and the partials fit the workspace.
   if (tid == 0) {
-    int64_t c = (int64_t)a.pps;
+    int64_t c;
     if (a.no_split) {
       c = INT_MAX;
     } else {
@@ -192,7 +225,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     const int64_t c = s_chunk;
     int64_t n_items = 0, n_part = 0;
     for (int i = tid; i < a.B; i += kPlanThreads) {
-      const SeqShape s = seq_shape(a, i);
+      const SeqShape s = shape(i);
       const int32_t ns = splits_for(s, c);
       n_items += (int64_t)ns * s.nrb;
       if (ns > 1) n_part += (int64_t)ns * a.Hkv * s.R;
@@ -218,7 +251,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     s.L = s.ql = s.npages = s.R = s.nrb = 0;
     int32_t ns = 0, qrows = 0;
     if (i < a.B) {
-      s = seq_shape(a, i);
+      s = shape(i);
       qrows = s.ql > 0 ? s.ql : 0;
       ns = splits_for(s, c);
     }
@@ -242,7 +275,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       sp.nsplit = (s.valid && fits) ? ns : 0;
       sp.nrb = s.nrb;
       sp.partial_base = (int32_t)my_part0;
-      sp.pad = 0;
+      sp.item0 = (int32_t)(my_item0 < a.items_cap ? my_item0 : 0);
       a.seqplan[i] = sp;
       for (int j = 0; j < qrows && my_row0 + j < a.T; ++j) a.token_seq[my_row0 + j] = i;
       if (ns > 0) {
@@ -261,6 +294,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
           }
         }
       }
+      if (sp.nsplit > 1)  // arrival counters of the last-split merge
+        for (int k = 0; k < s.nrb * a.Hkv; ++k) a.counters[(size_t)sp.item0 * a.Hkv + k] = 0;
     }
     carry_rows += t_rows;
     carry_items += t_items;
@@ -272,10 +307,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     a.header->chunk_pages = (int32_t)(c < INT_MAX ? c : INT_MAX);
     a.header->n_partial_rows = (int32_t)carry_part;
   }
+  __syncthreads();
+
+  // Rows owned by no sequence, or by one with inconsistent lengths, are NaN.
+  for (int r = tid; r < a.T; r += kPlanThreads) {
+    const int seq = a.token_seq[r];
+    if (seq >= 0 && !(a.seqplan[seq].flags & kSeqInvalid)) continue;
+    for (int h = 0; h < a.Hq; ++h) {
+      const size_t row = (size_t)r * a.Hq + h;
+      a.lse[row] = NAN;
+      if (a.is_bf16) {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.out) + row * a.D;
+        for (int d = 0; d < a.D; ++d) o[d] = __float2bfloat16(NAN);
+      } else {
+        float* o = static_cast<float*>(a.out) + row * a.D;
+        for (int d = 0; d < a.D; ++d) o[d] = NAN;
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------
-// Attention, bf16 storage: TMA page staging + mma.sync
+// Attention, bf16 storage
 // ------------------------------------------------------------------------------------
 struct AttnArgs {
   const void* q;
@@ -285,6 +338,7 @@ struct AttnArgs {
   const SeqPlan* seqplan;
   const Item* items;
   PlanHeader* header;
+  int32_t* counters;
   float* part_o;
   float* part_lse;
   const void* k_pages;  // fp32 path only
@@ -297,70 +351,184 @@ struct AttnArgs {
 
 template <int D>
 struct Smem {
-  static constexpr int NH = D / 64;                  // 128-byte column halves per row
-  static constexpr int kHalfBytes = kStageTokens * 128;
-  static constexpr int kOperandBytes = NH * kHalfBytes;  // K or V of one stage
+  static constexpr int NH = D / 64;                        // 128-byte halves per token row
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kOperandBytes = kStageTokens * kRowBytes;  // K or V of one stage
   static constexpr int kStageBytes = 2 * kOperandBytes;
-  static constexpr int kQStride = D * 2 + 16;            // padded Q row
+  static constexpr int kQStride = D * 2 + 16;               // padded Q row
   static constexpr int kQBytes = kRowBlock * kQStride;
-  static constexpr int kCombineFloats = (D / 8) * 4 + 4; // per thread: O frags + m,l x2
-  static constexpr int kCombineBytes = kConsumerWarps * 32 * kCombineFloats * 4;
-  static constexpr int kScratchBytes = kQBytes > kCombineBytes ? kQBytes : kCombineBytes;
-  static constexpr int kStagesOff = 0;
-  static constexpr int kScratchOff = kStages * kStageBytes;
-  static constexpr int kBarOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
-  // full[kStages], empty[kStages], ufull[kRing], uempty[kRing], ring_u[kRing], meta[kStages]
-  static constexpr int kBarBytes = (2 * kStages + 2 * kRing) * 8 + kRing * 4 + kStages * 4;
+  static constexpr int kNarrowStride = D + 4;               // floats per merge row
+  static constexpr int kNarrowWarpFloats = kNarrowRows * kNarrowStride + 2 * kNarrowRows;
+  static constexpr int kNarrowBytes = kConsumerWarps * kNarrowWarpFloats * 4;
+  static constexpr int kWideFloats = (D / 8) * 4 + 4;       // per thread: O frags + m,l x2
+  static constexpr int kWideBytes = kConsumerWarps * 32 * kWideFloats * 4;
+  static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
+  static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
+  static constexpr int kScratchOff = kSlots * kStageBytes;
+  static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
+  static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
+  // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing] | meta[kSlots], flag[4]
+  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing) * 8 + (kSlots + 4) * 4;
   static constexpr int kBytes = kBarOff + kBarBytes;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-// QK^T, online softmax and PV for one warp's token slice of one stage.
-// kbase / vbase: shared addresses of the stage's K and V (swizzled 128-byte rows).
-template <int D, int TS>
-__device__ __forceinline__ void stage_compute(uint32_t kbase, uint32_t vbase, int ts0,
-                                              int tvalid, const uint32_t (&qa)[D / 16][4],
-                                              float (&o)[D / 8][4], float (&m)[2],
-                                              float (&l)[2], int t_abs0, int limA, int limB,
-                                              bool need_mask, float scale_log2, int lane) {
-  constexpr int NT = TS / 8;
-  constexpr int kHalfBytes = Smem<D>::kHalfBytes;
-  const int g = lane >> 2, tq = lane & 3, mi = lane >> 3, r8 = lane & 7;
-  (void)g;
+// Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage:
+// the TMA box lands as [token][D/64 halves][64] with the 128-byte swizzle, i.e. the
+// chunk index is XOR-ed with the index of its 128-byte row modulo 8.
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int t, int gc) {
+  constexpr int NH = D / 64;
+  const int row = t * NH + (gc >> 3);
+  return (uint32_t)(row * 128 + (((gc & 7) ^ (row & 7)) << 4));
+}
 
+// ---- narrow units: S^T = K Q^T, one warp per stage -------------------------------
+template <int D, int NN>
+__device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int loaded,
+                                             const uint32_t (&qb)[D / 16][NN][2],
+                                             float (&oT)[D / 16][NN][4], float (&m)[NN][2],
+                                             float (&l)[NN][2], int t_abs0,
+                                             const int (&lim)[NN][2], bool need_mask,
+                                             float scale_log2, int lane) {
+  const int g = lane >> 2, mi = lane >> 3, r8 = lane & 7;
+  float s[2][NN][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    float acc[2][NN][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int nn = 0; nn < NN; ++nn) acc[h][nn][0] = acc[h][nn][1] = acc[h][nn][2] = acc[h][nn][3] = 0.f;
+    if (16 * mt < loaded) {
+      const int t = 16 * mt + (mi & 1) * 8 + r8;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(kbase + kv_off<D>(t, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(acc[ks & 1][nn], a, qb[ks][nn][0], qb[ks][nn][1]);
+      }
+    }
+#pragma unroll
+    for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[mt][nn][e] = acc[0][nn][e] + acc[1][nn][e];
+  }
+
+  // Scale to log2 units, mask, running max over the stage's tokens.
+  float mx[NN][2];
+#pragma unroll
+  for (int nn = 0; nn < NN; ++nn) mx[nn][0] = mx[nn][1] = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tt = 16 * mt + g + 8 * (e >> 1);
+        const bool off = tt >= loaded || (need_mask && t_abs0 + tt > lim[nn][e & 1]);
+        const float v = off ? -INFINITY : s[mt][nn][e] * scale_log2;
+        s[mt][nn][e] = v;
+        mx[nn][e & 1] = fmaxf(mx[nn][e & 1], v);
+      }
+  float muse[NN][2], alpha[NN][2];
+#pragma unroll
+  for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float v = mx[nn][h];
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      const float mnew = fmaxf(m[nn][h], v);
+      muse[nn][h] = mnew == -INFINITY ? 0.f : mnew;
+      alpha[nn][h] = exp2f(m[nn][h] - muse[nn][h]);
+      m[nn][h] = mnew;
+    }
+#pragma unroll
+  for (int nn = 0; nn < NN; ++nn) {
+    float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = exp2f(s[mt][nn][e] - muse[nn][e & 1]);
+        s[mt][nn][e] = p;
+        if (e & 1) rs1 += p;
+        else rs0 += p;
+      }
+    l[nn][0] = l[nn][0] * alpha[nn][0] + rs0;
+    l[nn][1] = l[nn][1] * alpha[nn][1] + rs1;
+  }
+#pragma unroll
+  for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+    for (int nn = 0; nn < NN; ++nn) {
+      oT[dt][nn][0] *= alpha[nn][0];
+      oT[dt][nn][1] *= alpha[nn][1];
+      oT[dt][nn][2] *= alpha[nn][0];
+      oT[dt][nn][3] *= alpha[nn][1];
+    }
+
+  // O^T += V^T P^T: the P^T operand is the transpose of the S^T accumulator tile.
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    if (16 * kk < loaded) {
+      uint32_t pb[NN][2];
+#pragma unroll
+      for (int nn = 0; nn < NN; ++nn) {
+        pb[nn][0] = movmatrix_trans(pack_bf16x2(s[kk][nn][0], s[kk][nn][1]));
+        pb[nn][1] = movmatrix_trans(pack_bf16x2(s[kk][nn][2], s[kk][nn][3]));
+      }
+      const int t = 16 * kk + (mi >> 1) * 8 + r8;
+#pragma unroll
+      for (int dt = 0; dt < D / 16; ++dt) {
+        uint32_t a[4];
+        ldsm_x4_trans(vbase + kv_off<D>(t, 2 * dt + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
+      }
+    }
+  }
+}
+
+// ---- wide units: S = Q K^T, warps split m16 row tiles and token slices --------------
+template <int D, int TS>
+__device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int ts0, int tvalid,
+                                           const uint32_t (&qa)[D / 16][4],
+                                           float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
+                                           int t_abs0, int limA, int limB, bool need_mask,
+                                           float scale_log2, int lane) {
+  constexpr int NT = TS / 8;
+  const int tq = lane & 3, mi = lane >> 3, r8 = lane & 7;
   float s[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     if (8 * nt < tvalid) {
-      const int t = ts0 + 8 * nt + r8;  // stage row this lane addresses
+      const int t = ts0 + 8 * nt + r8;
 #pragma unroll
       for (int qd = 0; qd < D / 32; ++qd) {
-        const int gc = 4 * qd + mi;  // 16-byte column chunk 0 .. D/8-1
-        const uint32_t addr =
-            kbase + (gc >> 3) * kHalfBytes + t * 128 + ((((gc & 7) ^ (t & 7))) << 4);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(addr, b0, b1, b2, b3);
+        ldsm_x4(kbase + kv_off<D>(t, 4 * qd + mi), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
         mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
       }
     }
   }
-
-  // Scale to log2 units, mask, running max.
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int tt = 8 * nt + 2 * tq + (e & 1);  // token within the slice
+      const int tt = 8 * nt + 2 * tq + (e & 1);
       const int lim = (e < 2) ? limA : limB;
       const bool off = tt >= tvalid || (need_mask && t_abs0 + ts0 + tt > lim);
       const float v = off ? -INFINITY : s[nt][e] * scale_log2;
       s[nt][e] = v;
       mx[e >> 1] = fmaxf(mx[e >> 1], v);
     }
-  }
   float alpha[2], muse[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -373,14 +541,13 @@ __device__ __forceinline__ void stage_compute(uint32_t kbase, uint32_t vbase, in
   }
   float rs[2] = {0.f, 0.f};
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float p = exp2f(s[nt][e] - muse[e >> 1]);
       s[nt][e] = p;
       rs[e >> 1] += p;
     }
-  }
   l[0] = l[0] * alpha[0] + rs[0];
   l[1] = l[1] * alpha[1] + rs[1];
 #pragma unroll
@@ -390,8 +557,6 @@ __device__ __forceinline__ void stage_compute(uint32_t kbase, uint32_t vbase, in
     o[dt][2] *= alpha[1];
     o[dt][3] *= alpha[1];
   }
-
-  // O += P V over 16-token k-steps.
 #pragma unroll
   for (int kk = 0; kk < TS / 16; ++kk) {
     if (16 * kk < tvalid) {
@@ -403,15 +568,95 @@ __device__ __forceinline__ void stage_compute(uint32_t kbase, uint32_t vbase, in
       const int t = ts0 + 16 * kk + (mi & 1) * 8 + r8;
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
-        const int gc = 2 * dp + (mi >> 1);
-        const uint32_t addr =
-            vbase + (gc >> 3) * kHalfBytes + t * 128 + ((((gc & 7) ^ (t & 7))) << 4);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(addr, b0, b1, b2, b3);
+        ldsm_x4_trans(vbase + kv_off<D>(t, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dp], pa, b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
+  }
+}
+
+// ---- output helpers ----------------------------------------------------------------
+__device__ __forceinline__ size_t out_row(const AttnArgs& a, const SeqPlan& sp, int head, int r) {
+  const int j = r / a.G, hh = r % a.G;
+  return (size_t)(sp.qrow0 + j) * a.Hq + (size_t)head * a.G + hh;
+}
+
+__device__ __forceinline__ size_t partial_row(const AttnArgs& a, const SeqPlan& sp, int split,
+                                              int head, int r) {
+  return (size_t)sp.partial_base + ((size_t)split * a.Hkv + head) * ((size_t)a.G * sp.qlen) + r;
+}
+
+// Merge the partials of every split of rows r0 .. r0+Rb-1 of one KV head (the caller is
+// the last split to finish: all partials are in memory).  Four consumer warps.
+template <int D>
+__device__ void merge_splits(const AttnArgs& a, const SeqPlan& sp, int head, int r0, int Rb,
+                             int warp, int lane) {
+  constexpr int E = D / 32;
+  const float kLn2 = 0.6931471805599453f;
+  for (int rr = warp; rr < Rb; rr += kConsumerWarps) {
+    const int r = r0 + rr;
+    float mx = -INFINITY;
+    bool bad = false;
+    for (int s = lane; s < sp.nsplit; s += 32) {
+      const float v = __ldcg(a.part_lse + partial_row(a, sp, s, head, r));
+      bad |= isnan(v);
+      mx = fmaxf(mx, v);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    bad = __any_sync(0xffffffffu, bad);
+    const float mu = mx == -INFINITY ? 0.f : mx;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    for (int s = 0; s < sp.nsplit; ++s) {
+      const size_t pr = partial_row(a, sp, s, head, r);
+      const float w = exp2f((__ldcg(a.part_lse + pr) - mu) * 1.4426950408889634f);
+      wsum += w;
+      const float* po = a.part_o + pr * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
+    const float inv = 1.f / wsum;
+    const size_t orow = out_row(a, sp, head, r);
+    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + orow * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const float x0 = bad ? NAN : acc[e] * inv, x1 = bad ? NAN : acc[e + 1] * inv;
+      *reinterpret_cast<uint32_t*>(og + e) = pack_bf16x2(x0, x1);
+    }
+    if (lane == 0) a.lse[orow] = bad ? NAN : mu + log2f(wsum) * kLn2;
+  }
+}
+
+// After this CTA wrote its partial rows: count the arrival; the last split merges.
+template <int D>
+__device__ __forceinline__ void finish_split(const AttnArgs& a, const SeqPlan& sp,
+                                             const Item& it, int head, int r0, int Rb,
+                                             int32_t* flag, int warp, int lane) {
+  __threadfence();
+  named_bar_sync(1, kConsumerThreads);
+  if (threadIdx.x == 0) {
+    const int rb = it.split_rb & ((1 << kRbBits) - 1);
+    int32_t* cnt = a.counters + ((size_t)sp.item0 + rb) * a.Hkv + head;
+    *flag = atomicAdd(cnt, 1) == sp.nsplit - 1;
+  }
+  named_bar_sync(1, kConsumerThreads);
+  if (*flag) {
+    __threadfence();
+    merge_splits<D>(a, sp, head, r0, Rb, warp, lane);
   }
 }
 
@@ -421,22 +666,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using S = Smem<D>;
   constexpr int PPS = kStageTokens / P;  // pages per stage
-  constexpr int kPageBytes = P * 128;    // one column half of one page of one head
+  constexpr int kPageBytes = P * D * 2;  // one page of one head, one operand
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* stages = smem + S::kStagesOff;
+  uint8_t* stages = smem;
   uint8_t* scratch = smem + S::kScratchOff;
+  RingEntry* ring = reinterpret_cast<RingEntry*>(smem + S::kRingOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
-  uint64_t* empty = full + kStages;
-  uint64_t* ufull = empty + kStages;
+  uint64_t* empty = full + kSlots;
+  uint64_t* ufull = empty + kSlots;
   uint64_t* uempty = ufull + kRing;
-  int32_t* ring_u = reinterpret_cast<int32_t*>(uempty + kRing);
-  int32_t* meta = ring_u + kRing;
+  int32_t* meta = reinterpret_cast<int32_t*>(uempty + kRing);
+  int32_t* flag = meta + kSlots;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -446,297 +692,463 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_fence_init();
   }
+  if (warp == kConsumerWarps && lane == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+  }
   __syncthreads();
+  pdl_wait_prior_grid();  // the plan of this call is complete and visible
 
   const int32_t n_units = a.header->n_items * a.Hkv;
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      prefetch_tensor_map(&tm_k);
-      prefetch_tensor_map(&tm_v);
-    }
     const uint64_t pol = l2_policy_evict_first();
     uint32_t stage_it = 0, unit_it = 0;
-    int32_t u_next = 0;
-    if (lane == 0) u_next = atomicAdd(&a.header->work_counter, 1);
     bool ok = true;
+    // Descriptor pipeline: unit u is streamed while the next unit's descriptor and
+    // first block-table chunk are in flight, and the atomic for the one after.
+    int32_t u = 0, u1 = 0, u2_lane0 = 0;
+    if (lane == 0) {
+      u = atomicAdd(&a.header->work_counter, 1);
+      u1 = atomicAdd(&a.header->work_counter, 1);
+    }
+    u = __shfl_sync(0xffffffffu, u, 0);
+    u1 = __shfl_sync(0xffffffffu, u1, 0);
+    Item it{}, it1{};
+    SeqPlan sp{}, sp1{};
+    if (u < n_units) {
+      it = a.items[u / a.Hkv];
+      if (it.seq >= 0) sp = a.seqplan[it.seq];
+    }
+    if (u1 < n_units) {
+      it1 = a.items[u1 / a.Hkv];
+      if (it1.seq >= 0) sp1 = a.seqplan[it1.seq];
+    }
+    if (lane == 0) u2_lane0 = atomicAdd(&a.header->work_counter, 1);
+    int32_t bt_cur = 0;  // this lane's block-table entry of the unit's first 32 pages
+    if (u < n_units && it.seq >= 0 && it.page_begin + lane < it.page_end)
+      bt_cur = a.block_table[(size_t)it.seq * a.maxp + it.page_begin + lane];
     for (;;) {
-      const int32_t u = __shfl_sync(0xffffffffu, u_next, 0);
       const int slot = unit_it % kRing;
       ok = mbar_wait(&uempty[slot], ((unit_it / kRing) & 1) ^ 1);
       if (!ok) break;
       if (u >= n_units) {
         if (lane == 0) {
-          ring_u[slot] = -1;
+          ring[slot].u = -1;
           mbar_arrive(&ufull[slot]);
         }
         break;
       }
       if (lane == 0) {
-        u_next = atomicAdd(&a.header->work_counter, 1);  // next unit, consumed next pass
-        ring_u[slot] = u;
+        RingEntry e;
+        e.u = u;
+        e.head = u % a.Hkv;
+        e.item = it;
+        e.sp = sp;
+        e.pad[0] = e.pad[1] = 0;
+        ring[slot] = e;
         mbar_arrive(&ufull[slot]);
       }
       ++unit_it;
-      const Item it = a.items[u / a.Hkv];
-      const int head = u % a.Hkv;
-      if (it.seq < 0) continue;
-      const int32_t* bt_row = a.block_table + (size_t)it.seq * a.maxp;
-      for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
-        const int npg = min(32, it.page_end - pg0);
-        const int32_t my_id = lane < npg ? bt_row[pg0 + lane] : 0;
-        for (int s0 = 0; s0 < npg; s0 += PPS) {
-          const int stage = stage_it % kStages;
-          ok = mbar_wait(&empty[stage], ((stage_it / kStages) & 1) ^ 1);
-          if (!ok) break;
-          const int n_in = min(PPS, npg - s0);
-          int ids[PPS];
-          uint32_t bytes = 0;
-          int bad = 0;
-#pragma unroll
-          for (int e = 0; e < PPS; ++e) {
-            ids[e] = __shfl_sync(0xffffffffu, my_id, (s0 + e) & 31);
-            if (e < n_in) {
-              if (ids[e] < 0 || ids[e] >= a.num_pages) bad = 1;
-              else bytes += 2u * S::NH * kPageBytes;
-            }
-          }
-          if (lane == 0) {
-            meta[stage] = bad;
-            mbar_arrive_expect_tx(&full[stage], bytes);
-            uint8_t* kdst = stages + stage * S::kStageBytes;
-            uint8_t* vdst = kdst + S::kOperandBytes;
+      // Prefetch the next unit's first block-table chunk and the descriptor after it.
+      int32_t bt_next = 0;
+      if (u1 < n_units && it1.seq >= 0 && it1.page_begin + lane < it1.page_end)
+        bt_next = a.block_table[(size_t)it1.seq * a.maxp + it1.page_begin + lane];
+      const int32_t u2 = __shfl_sync(0xffffffffu, u2_lane0, 0);
+      Item it2{};
+      SeqPlan sp2{};
+      if (u2 < n_units) it2 = a.items[u2 / a.Hkv];
+      if (lane == 0) u2_lane0 = atomicAdd(&a.header->work_counter, 1);
+
+      if (it.seq >= 0) {
+        const int head = u % a.Hkv;
+        const int32_t* bt_row = a.block_table + (size_t)it.seq * a.maxp;
+        for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
+          const int npg = min(32, it.page_end - pg0);
+          const int32_t my_id =
+              pg0 == it.page_begin ? bt_cur : (lane < npg ? bt_row[pg0 + lane] : 0);
+          for (int s0 = 0; s0 < npg; s0 += PPS) {
+            const int slot_s = stage_it % kSlots;
+            ok = mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1);
+            if (!ok) break;
+            const int n_in = min(PPS, npg - s0);
+            int ids[PPS];
+            uint32_t bytes = 0;
+            int bad = 0;
 #pragma unroll
             for (int e = 0; e < PPS; ++e) {
-              if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
+              ids[e] = __shfl_sync(0xffffffffu, my_id, (s0 + e) & 31);
+              if (e < n_in) {
+                if (ids[e] < 0 || ids[e] >= a.num_pages) bad = 1;
+                else bytes += 2u * kPageBytes;
+              }
+            }
+            if (lane == 0) {
+              meta[slot_s] = bad;
+              mbar_arrive_expect_tx(&full[slot_s], bytes);
+              uint8_t* kdst = stages + slot_s * S::kStageBytes;
+              uint8_t* vdst = kdst + S::kOperandBytes;
 #pragma unroll
-                for (int h = 0; h < S::NH; ++h) {
-                  const int off = h * S::kHalfBytes + e * kPageBytes;
-                  tma_load_3d(kdst + off, &tm_k, &full[stage], h * 64, head, ids[e] * P, pol);
-                  tma_load_3d(vdst + off, &tm_v, &full[stage], h * 64, head, ids[e] * P, pol);
+              for (int e = 0; e < PPS; ++e) {
+                if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
+                  tma_load_4d(kdst + e * kPageBytes, &tm_k, &full[slot_s], 0, 0, head, ids[e] * P, pol);
+                  tma_load_4d(vdst + e * kPageBytes, &tm_v, &full[slot_s], 0, 0, head, ids[e] * P, pol);
                 }
               }
             }
+            __syncwarp();
+            ++stage_it;
           }
-          __syncwarp();
-          ++stage_it;
         }
       }
       if (!ok) break;
+      if (u2 < n_units && it2.seq >= 0) sp2 = a.seqplan[it2.seq];
+      u = u1;
+      it = it1;
+      sp = sp1;
+      bt_cur = bt_next;
+      u1 = u2;
+      it1 = it2;
+      sp1 = sp2;
     }
     if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
     // Let every copy this warp issued land before the CTA can exit.
-    for (uint32_t d = stage_it > kStages ? stage_it - kStages : 0; d < stage_it; ++d)
-      mbar_wait(&full[d % kStages], (d / kStages) & 1);
+    for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
+      mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
     return;
   }
 
   // -------------------------------- consumers --------------------------------
   const int tid = threadIdx.x;  // 0 .. kConsumerThreads-1
   const int g = lane >> 2, tq = lane & 3;
+  const float kLn2 = 0.6931471805599453f;
   uint32_t stage_it = 0, unit_it = 0;
+  bool timed_out = false;
   for (;;) {
     const int slot = unit_it % kRing;
-    if (!mbar_wait(&ufull[slot], (unit_it / kRing) & 1)) {
-      if (lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
+    const bool got = mbar_wait(&ufull[slot], (unit_it / kRing) & 1);
+    RingEntry re;
+    re.u = -1;
+    if (got) re = ring[slot];
+    __syncwarp();
+    if (lane == 0 && got) mbar_arrive(&uempty[slot]);
+    ++unit_it;
+    // Every consumer warp takes the same decision (a warp that left alone would strand
+    // the others at a named barrier); this barrier also frees the scratch area of the
+    // previous unit's merge for the next query rows.
+    if (named_bar_or(1, kConsumerThreads, !got)) {
+      timed_out = true;
       break;
     }
-    const int32_t u = ring_u[slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&uempty[slot]);
-    ++unit_it;
-    if (u < 0) break;
-
-    const Item it = a.items[u / a.Hkv];
+    if (re.u < 0) break;
+    const Item it = re.item;
     if (it.seq < 0) continue;
-    const int head = u % a.Hkv;
-    const SeqPlan sp = a.seqplan[it.seq];
+    const SeqPlan sp = re.sp;
+    const int head = re.head;
     const int split = it.split_rb >> kRbBits, rb = it.split_rb & ((1 << kRbBits) - 1);
     const int L = sp.len, ql = sp.qlen;
     const int R = a.G * ql;
     const int r0 = rb * kRowBlock;
     const int Rb = min(kRowBlock, R - r0);
-    const int nM = (Rb + 15) >> 4;
-    const int nW = nM == 1 ? 4 : (nM == 2 ? 2 : 1);
-    const bool active = warp < nM * nW;
-    const int mt = warp % nM;
-    const int slice = warp / nM;
-    const int TS = kStageTokens / nW;
+    const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
+    const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
 
-    // Stage the unit's query rows (row r: token r / G, head head * G + r % G).
-    named_bar_sync(1, kConsumerThreads);
+    // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
+    // past Rb up to the MMA tile are zero.
     {
       constexpr int kChunks = D / 8;
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-      for (int c = tid; c < kRowBlock * kChunks; c += kConsumerThreads) {
+      const int rows_pad = Rb <= 8 ? 8 : ((Rb + 15) & ~15);
+      for (int c = tid; c < rows_pad * kChunks; c += kConsumerThreads) {
         const int row = c / kChunks, ch = c % kChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < Rb) {
-          const int r = r0 + row;
-          const int j = r / a.G, hh = r % a.G;
-          const size_t src = ((size_t)(sp.qrow0 + j) * a.Hq + (size_t)head * a.G + hh) * D + ch * 8;
-          v = *reinterpret_cast<const uint4*>(qg + src);
-        }
+        if (row < Rb)
+          v = *reinterpret_cast<const uint4*>(qg + out_row(a, sp, head, r0 + row) * D + ch * 8);
         *reinterpret_cast<uint4*>(scratch + row * S::kQStride + ch * 16) = v;
       }
     }
     named_bar_sync(1, kConsumerThreads);
-    uint32_t qa[D / 16][4];
-    if (active) {
-      const int mi = lane >> 3;
-      const int row = 16 * mt + (mi & 1) * 8 + (lane & 7);
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int ch = 2 * ks + (mi >> 1);
-        ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qa[ks][0], qa[ks][1], qa[ks][2],
-                qa[ks][3]);
-      }
-    }
 
-    float o[D / 8][4];
+    bool poison = false;
+    if (Rb <= kNarrowRows) {
+      // ============================ narrow unit ============================
+      auto run = [&](auto nn_tag) {
+        constexpr int NN = decltype(nn_tag)::value;
+        uint32_t qb[D / 16][NN][2];
 #pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    const int rA = r0 + 16 * mt + g, rB = rA + 8;
-    const int limA = rA < R ? L - ql + rA / a.G : L - 1;
-    const int limB = rB < R ? L - ql + rB / a.G : L - 1;
-    const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
-    bool poison = false, timed_out = false;
-
-    for (int pg = it.page_begin; pg < it.page_end; pg += PPS) {
-      const int stage = stage_it % kStages;
-      if (!mbar_wait(&full[stage], (stage_it / kStages) & 1)) {
-        timed_out = true;
-        break;
-      }
-      ++stage_it;
-      if (meta[stage]) poison = true;
-      const int loaded = min(PPS, it.page_end - pg) * P;
-      const int t_abs0 = pg * P;
-      const uint32_t kbase = smem_u32(stages + stage * S::kStageBytes);
-      const uint32_t vbase = kbase + S::kOperandBytes;
-      if (active) {
-        const int ts0 = slice * TS;
-        const int tvalid = min(TS, loaded - ts0);
-        if (tvalid > 0) {
-          // Pool slots past the end of the sequence may hold anything: zero their V
-          // rows so that a zero attention weight cannot meet a NaN.
-          if (t_abs0 + ts0 + tvalid > L) {
-            const int z0 = max(0, L - t_abs0 - ts0);
-            uint8_t* vrow = stages + stage * S::kStageBytes + S::kOperandBytes;
-            for (int c = z0 * 8 * S::NH + lane; c < tvalid * 8 * S::NH; c += 32) {
-              const int t = ts0 + c / (8 * S::NH), rem = c % (8 * S::NH);
-              *reinterpret_cast<uint4*>(vrow + (rem >> 3) * S::kHalfBytes + t * 128 +
-                                        (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
-            }
+        for (int kp = 0; kp < D / 32; ++kp)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn) {
+            const int row = 8 * nn + (lane & 7);
+            const int ch = 4 * kp + (lane >> 3);
+            ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qb[2 * kp][nn][0],
+                    qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0], qb[2 * kp + 1][nn][1]);
+          }
+        float oT[D / 16][NN][4];
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn) oT[dt][nn][0] = oT[dt][nn][1] = oT[dt][nn][2] = oT[dt][nn][3] = 0.f;
+        float m[NN][2], l[NN][2];
+        int lim[NN][2];
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            m[nn][e] = -INFINITY;
+            l[nn][e] = 0.f;
+            const int row = 8 * nn + 2 * tq + e;
+            lim[nn][e] = row < Rb ? L - ql + (r0 + row) / a.G : L - 1;
+          }
+        for (int si = 0; si < n_stages; ++si, ++stage_it) {
+          if ((int)(stage_it % kConsumerWarps) != warp) continue;
+          const int slot_s = stage_it % kSlots;
+          if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+            timed_out = true;
+            stage_it += n_stages - si;
+            break;
+          }
+          if (meta[slot_s]) poison = true;
+          const int pg = it.page_begin + si * PPS;
+          const int loaded = min(PPS, it.page_end - pg) * P;
+          const int t_abs0 = pg * P;
+          const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
+          const uint32_t vbase = kbase + S::kOperandBytes;
+          if (t_abs0 + loaded > L) {
+            // Pool slots past the end of the sequence may hold anything: zero their V
+            // rows so that a zero attention weight cannot meet a NaN.
+            uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+            const int z0 = max(0, L - t_abs0);
+            for (int c = z0 * (D / 8) + lane; c < loaded * (D / 8); c += 32)
+              *reinterpret_cast<uint4*>(vrow + kv_off<D>(c / (D / 8), c % (D / 8))) =
+                  make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
             __syncwarp();
           }
-          const bool need_mask = t_abs0 + ts0 + tvalid - 1 > min_lim;
-          if (TS == 16)
-            stage_compute<D, 16>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
-                                 need_mask, a.scale_log2, lane);
-          else if (TS == 32)
-            stage_compute<D, 32>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
-                                 need_mask, a.scale_log2, lane);
-          else
-            stage_compute<D, 64>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
-                                 need_mask, a.scale_log2, lane);
+          const bool need_mask = t_abs0 + loaded - 1 > min_lim;
+          narrow_stage<D, NN>(kbase, vbase, loaded, qb, oT, m, l, t_abs0, lim, need_mask,
+                              a.scale_log2, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_count(&empty[slot_s], kConsumerWarps);
+        }
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 4);
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 8);
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 16);
+          }
+        // Merge the four warps' states through shared memory.
+        named_bar_sync(1, kConsumerThreads);  // all warps are done with the Q rows
+        float* wb = reinterpret_cast<float*>(scratch) + (size_t)warp * S::kNarrowWarpFloats;
+        // Rows a warp never touched keep m = -inf, l = 0 and contribute nothing.
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wb[(8 * nn + 2 * tq + (e & 1)) * S::kNarrowStride + 16 * dt + g + 8 * (e >> 1)] =
+                  oT[dt][nn][e];
+        if (g == 0)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              wb[kNarrowRows * S::kNarrowStride + 8 * nn + 2 * tq + e] = m[nn][e];
+              wb[kNarrowRows * S::kNarrowStride + kNarrowRows + 8 * nn + 2 * tq + e] = l[nn][e];
+            }
+      };
+      if (Rb <= 8) run(std::integral_constant<int, 1>{});
+      else run(std::integral_constant<int, 2>{});
+      // Bad pages and timeouts seen by any warp's stages concern the whole unit.
+      poison = named_bar_or(1, kConsumerThreads, poison);
+      if (named_bar_or(1, kConsumerThreads, timed_out)) {
+        timed_out = true;
+        break;
+      }
+      const float* buf = reinterpret_cast<const float*>(scratch);
+      const int d = warp * 32 + lane;  // this lane's output column
+      for (int r = 0; r < Rb; ++r) {
+        float mw[kConsumerWarps], M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          mw[w] = buf[w * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + r];
+          M = fmaxf(M, mw[w]);
+        }
+        const float mu = M == -INFINITY ? 0.f : M;
+        float Lsum = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = exp2f(mw[w] - mu);
+          Lsum += f * buf[w * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + kNarrowRows + r];
+          if (d < D) acc += f * buf[w * S::kNarrowWarpFloats + r * S::kNarrowStride + d];
+        }
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        float row_lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+        float x = acc * inv;
+        if (poison) row_lse = x = NAN;
+        if (sp.nsplit == 1) {
+          const size_t orow = out_row(a, sp, head, r0 + r);
+          if (d < D) static_cast<__nv_bfloat16*>(a.out)[orow * D + d] = __float2bfloat16(x);
+          if (warp == 0 && lane == 0) a.lse[orow] = row_lse;
+        } else {
+          const size_t prow = partial_row(a, sp, split, head, r0 + r);
+          if (d < D) a.part_o[prow * D + d] = x;
+          if (warp == 0 && lane == 0) a.part_lse[prow] = row_lse;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-    }
-    if (timed_out) {
-      if (lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
-      break;
-    }
-
-    // Row sums across the quad that shares a row.
+    } else {
+      // ============================= wide unit =============================
+      const int nM = (Rb + 15) >> 4;
+      const int nW = nM == 2 ? 2 : 1;
+      const bool active = warp < nM * nW;
+      const int mt = warp % nM;
+      const int slice = warp / nM;
+      const int TS = kStageTokens / nW;
+      uint32_t qa[D / 16][4];
+      if (active) {
+        const int mi = lane >> 3;
+        const int row = 16 * mt + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
-    }
-
-    // Merge the token slices of one m-tile (nW warps) through shared memory.
-    float* cb = reinterpret_cast<float*>(scratch);
-    named_bar_sync(1, kConsumerThreads);  // everyone is done with the Q rows
-    if (active && nW > 1 && slice > 0) {
-      float* mine = cb + (size_t)warp * 32 * S::kCombineFloats;
-#pragma unroll
-      for (int dt = 0; dt < D / 8; ++dt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) mine[(dt * 4 + e) * 32 + lane] = o[dt][e];
-      mine[(D / 2 + 0) * 32 + lane] = m[0];
-      mine[(D / 2 + 1) * 32 + lane] = m[1];
-      mine[(D / 2 + 2) * 32 + lane] = l[0];
-      mine[(D / 2 + 3) * 32 + lane] = l[1];
-    }
-    named_bar_sync(1, kConsumerThreads);
-    if (active && slice == 0) {
-      for (int sl = 1; sl < nW; ++sl) {
-        const float* other = cb + (size_t)(mt + sl * nM) * 32 * S::kCombineFloats;
-        float om[2] = {other[(D / 2 + 0) * 32 + lane], other[(D / 2 + 1) * 32 + lane]};
-        float ol[2] = {other[(D / 2 + 2) * 32 + lane], other[(D / 2 + 3) * 32 + lane]};
-        float fa[2], fb[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float mm = fmaxf(m[h], om[h]);
-          const float mu = mm == -INFINITY ? 0.f : mm;
-          fa[h] = exp2f(m[h] - mu);
-          fb[h] = exp2f(om[h] - mu);
-          l[h] = l[h] * fa[h] + ol[h] * fb[h];
-          m[h] = mm;
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int ch = 2 * ks + (mi >> 1);
+          ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qa[ks][0], qa[ks][1],
+                  qa[ks][2], qa[ks][3]);
         }
+      }
+      float o[D / 8][4];
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      const int rA = r0 + 16 * mt + g, rB = rA + 8;
+      const int limA = rA < R ? L - ql + rA / a.G : L - 1;
+      const int limB = rB < R ? L - ql + rB / a.G : L - 1;
+      for (int si = 0; si < n_stages; ++si, ++stage_it) {
+        const int slot_s = stage_it % kSlots;
+        if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+          timed_out = true;
+          stage_it += n_stages - si;
+          break;
+        }
+        if (meta[slot_s]) poison = true;
+        const int pg = it.page_begin + si * PPS;
+        const int loaded = min(PPS, it.page_end - pg) * P;
+        const int t_abs0 = pg * P;
+        const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
+        const uint32_t vbase = kbase + S::kOperandBytes;
+        if (active) {
+          const int ts0 = slice * TS;
+          const int tvalid = min(TS, loaded - ts0);
+          if (tvalid > 0) {
+            if (t_abs0 + ts0 + tvalid > L) {
+              // Several warps read these rows: each zeroes them before its own reads
+              // (all write the same zeros).
+              uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+              const int z0 = max(0, L - t_abs0 - ts0);
+              for (int c = z0 * (D / 8) + lane; c < tvalid * (D / 8); c += 32)
+                *reinterpret_cast<uint4*>(vrow + kv_off<D>(ts0 + c / (D / 8), c % (D / 8))) =
+                    make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            const bool need_mask = t_abs0 + ts0 + tvalid - 1 > min_lim;
+            if (TS == 16)
+              wide_stage<D, 16>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
+                                need_mask, a.scale_log2, lane);
+            else
+              wide_stage<D, 32>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
+                                need_mask, a.scale_log2, lane);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot_s]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+      }
+      float* cb = reinterpret_cast<float*>(scratch);
+      named_bar_sync(1, kConsumerThreads);  // everyone is done with the Q rows
+      if (active && nW > 1 && slice > 0) {
+        float* mine = cb + (size_t)warp * 32 * S::kWideFloats;
 #pragma unroll
         for (int dt = 0; dt < D / 8; ++dt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            o[dt][e] = o[dt][e] * fa[e >> 1] + other[(dt * 4 + e) * 32 + lane] * fb[e >> 1];
+          for (int e = 0; e < 4; ++e) mine[(dt * 4 + e) * 32 + lane] = o[dt][e];
+        mine[(D / 2 + 0) * 32 + lane] = m[0];
+        mine[(D / 2 + 1) * 32 + lane] = m[1];
+        mine[(D / 2 + 2) * 32 + lane] = l[0];
+        mine[(D / 2 + 3) * 32 + lane] = l[1];
       }
-
-      // Write: the final rows (one split) or this split's normalised partial.
-      const float kLn2 = 0.6931471805599453f;
+      poison = named_bar_or(1, kConsumerThreads, poison);
+      if (named_bar_or(1, kConsumerThreads, timed_out)) {
+        timed_out = true;
+        break;
+      }
+      if (active && slice == 0) {
+        for (int sl = 1; sl < nW; ++sl) {
+          const float* other = cb + (size_t)(mt + sl * nM) * 32 * S::kWideFloats;
+          const float om[2] = {other[(D / 2 + 0) * 32 + lane], other[(D / 2 + 1) * 32 + lane]};
+          const float ol[2] = {other[(D / 2 + 2) * 32 + lane], other[(D / 2 + 3) * 32 + lane]};
+          float fa[2], fb[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = h ? rB : rA;
-        if (r >= r0 + Rb) continue;
-        const int j = r / a.G, hh = r % a.G;
-        const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-        float row_lse = l[h] > 0.f ? (m[h] + log2f(l[h])) * kLn2 : -INFINITY;
-        if (poison) row_lse = NAN;
-        if (sp.nsplit == 1) {
-          const size_t orow = (size_t)(sp.qrow0 + j) * a.Hq + (size_t)head * a.G + hh;
-          __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + orow * D;
-#pragma unroll
-          for (int dt = 0; dt < D / 8; ++dt) {
-            float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
-            if (poison) x0 = x1 = NAN;
-            *reinterpret_cast<uint32_t*>(og + dt * 8 + 2 * tq) = pack_bf16x2(x0, x1);
+          for (int h = 0; h < 2; ++h) {
+            const float mm = fmaxf(m[h], om[h]);
+            const float mu = mm == -INFINITY ? 0.f : mm;
+            fa[h] = exp2f(m[h] - mu);
+            fb[h] = exp2f(om[h] - mu);
+            l[h] = l[h] * fa[h] + ol[h] * fb[h];
+            m[h] = mm;
           }
-          if (tq == 0) a.lse[orow] = row_lse;
-        } else {
-          const size_t prow =
-              (size_t)sp.partial_base + ((size_t)split * a.Hkv + head) * R + r;
-          float* po = a.part_o + prow * D;
 #pragma unroll
-          for (int dt = 0; dt < D / 8; ++dt) {
-            float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
-            if (poison) x0 = x1 = NAN;
-            *reinterpret_cast<float2*>(po + dt * 8 + 2 * tq) = make_float2(x0, x1);
+          for (int dt = 0; dt < D / 8; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[dt][e] = o[dt][e] * fa[e >> 1] + other[(dt * 4 + e) * 32 + lane] * fb[e >> 1];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = h ? rB : rA;
+          if (r >= r0 + Rb) continue;
+          const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+          float row_lse = l[h] > 0.f ? (m[h] + log2f(l[h])) * kLn2 : -INFINITY;
+          if (poison) row_lse = NAN;
+          if (sp.nsplit == 1) {
+            const size_t orow = out_row(a, sp, head, r);
+            __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + orow * D;
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) {
+              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
+              if (poison) x0 = x1 = NAN;
+              *reinterpret_cast<uint32_t*>(og + dt * 8 + 2 * tq) = pack_bf16x2(x0, x1);
+            }
+            if (tq == 0) a.lse[orow] = row_lse;
+          } else {
+            const size_t prow = partial_row(a, sp, split, head, r);
+            float* po = a.part_o + prow * D;
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) {
+              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
+              if (poison) x0 = x1 = NAN;
+              *reinterpret_cast<float2*>(po + dt * 8 + 2 * tq) = make_float2(x0, x1);
+            }
+            if (tq == 0) a.part_lse[prow] = row_lse;
           }
-          if (tq == 0) a.part_lse[prow] = row_lse;
         }
       }
     }
     if (poison && tid == 0) atomicOr(a.err, VAS_DEV_BAD_PAGE);
+    if (sp.nsplit > 1) finish_split<D>(a, sp, it, head, r0, Rb, flag, warp, lane);
   }
+  if (timed_out && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
 }
 
 // ------------------------------------------------------------------------------------
-// Attention, fp32 storage: one warp per query row on the CUDA cores
+// Attention, fp32 storage: one warp per query row on the CUDA cores (no split)
 // ------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
@@ -747,6 +1159,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   const float* vp = static_cast<const float*>(a.v_pages);
   float* og = static_cast<float*>(a.out);
   __shared__ float qs[4][D];
+  pdl_wait_prior_grid();
   const int32_t n_units = a.header->n_items * a.Hkv;
   for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Item it = a.items[u / a.Hkv];
@@ -757,9 +1170,9 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
     const int L = sp.len, ql = sp.qlen, R = a.G * ql;
     const int32_t* bt_row = a.block_table + (size_t)it.seq * a.maxp;
     for (int r = rb * kRowBlock + warp; r < min(R, rb * kRowBlock + kRowBlock); r += 4) {
-      const int j = r / a.G, hh = r % a.G;
+      const int j = r / a.G;
       const int pos = L - ql + j;
-      const size_t orow = (size_t)(sp.qrow0 + j) * a.Hq + (size_t)head * a.G + hh;
+      const size_t orow = out_row(a, sp, head, r);
       __syncwarp();
 #pragma unroll
       for (int e = 0; e < E; ++e) qs[warp][lane + 32 * e] = qg[orow * D + lane + 32 * e];
@@ -823,90 +1236,6 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
 }
 
 // ------------------------------------------------------------------------------------
-// LSE merge of split partials; NaN fill of rows a device-detected error left undefined
-// ------------------------------------------------------------------------------------
-struct CombineArgs {
-  const SeqPlan* seqplan;
-  const int32_t* token_seq;
-  const float* part_o;
-  const float* part_lse;
-  void* out;
-  float* lse;
-  int32_t T, Hq, Hkv, G, D, is_bf16;
-};
-
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + warp;  // (token, q head)
-  if (row >= (int64_t)a.T * a.Hq) return;
-  const int token = (int)(row / a.Hq), h = (int)(row % a.Hq);
-  const int seq = a.token_seq[token];
-  SeqPlan sp;
-  bool nan_fill = seq < 0;
-  if (!nan_fill) {
-    sp = a.seqplan[seq];
-    if (sp.flags & kSeqInvalid) nan_fill = true;
-    else if (sp.nsplit <= 1) return;  // written by the attention kernel
-  }
-  float outv[4];
-  float row_lse;
-  if (nan_fill) {
-    outv[0] = outv[1] = outv[2] = outv[3] = NAN;
-    row_lse = NAN;
-  } else {
-    const int j = token - sp.qrow0, g = h / a.G, hh = h % a.G;
-    const int R = a.G * sp.qlen, r = j * a.G + hh;
-    const int ns = sp.nsplit;
-    auto prow = [&](int s) -> size_t {
-      return (size_t)sp.partial_base + ((size_t)s * a.Hkv + g) * R + r;
-    };
-    float mx = -INFINITY;
-    bool any_nan = false;
-    for (int s = lane; s < ns; s += 32) {
-      const float v = a.part_lse[prow(s)];
-      any_nan |= isnan(v);
-      mx = fmaxf(mx, v);
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    any_nan = __any_sync(0xffffffffu, any_nan);
-    const float mu = mx == -INFINITY ? 0.f : mx;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float wsum = 0.f;
-    const int E = a.D / 32;  // 2 or 4 elements per lane
-    for (int s = 0; s < ns; ++s) {
-      const float w = expf(a.part_lse[prow(s)] - mu);
-      wsum += w;
-      const float* po = a.part_o + prow(s) * a.D + lane * E;
-      if (E == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(po);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(po);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-      }
-    }
-    const float inv = 1.f / wsum;
-    for (int e = 0; e < 4; ++e) outv[e] = any_nan ? NAN : acc[e] * inv;
-    row_lse = any_nan ? NAN : mu + logf(wsum);
-  }
-  const int E = a.D / 32;
-  if (a.is_bf16) {
-    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + row * a.D + lane * E;
-    for (int e = 0; e < E; e += 2)
-      *reinterpret_cast<uint32_t*>(og + e) = pack_bf16x2(outv[e], outv[e + 1]);
-  } else {
-    float* og = static_cast<float*>(a.out) + row * a.D + lane * E;
-    for (int e = 0; e < E; ++e) og[e] = outv[e];
-  }
-  if (lane == 0) a.lse[row] = row_lse;
-}
-
-// ------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------
 bool dims_ok(const vas_attn_dims* d) {
@@ -941,6 +1270,8 @@ Layout make_layout(const vas_attn_dims* d, int64_t items_cap, int64_t partial_ca
   off = align_up(off + (size_t)d->total_q_tokens * 4, 256);
   L.items = off;
   off = align_up(off + (size_t)items_cap * sizeof(Item), 256);
+  L.counters = off;
+  off = align_up(off + (size_t)items_cap * d->num_kv_heads * 4, 256);
   L.part_lse = off;
   off = align_up(off + (size_t)partial_cap * 4, 256);
   L.part_o = off;
@@ -983,17 +1314,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 3-D view of a page pool: (D, Hkv, num_pages * P) with a (64, 1, P) box, 128B swizzle.
+// 4-D view of a page pool: (64, D/64, Hkv, num_pages * P) with a (64, D/64, 1, P) box --
+// one page of one KV head -- and the 128-byte swizzle.
 bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d) {
   auto fn = get_encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_kv_heads,
+  const cuuint64_t dims[4] = {64, (cuuint64_t)d->head_dim / 64, (cuuint64_t)d->num_kv_heads,
                               (cuuint64_t)d->num_pages * d->page_size};
-  const cuuint64_t strides[2] = {(cuuint64_t)d->head_dim * 2,
+  const cuuint64_t strides[3] = {128, (cuuint64_t)d->head_dim * 2,
                                  (cuuint64_t)d->num_kv_heads * d->head_dim * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)d->page_size};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  const cuuint32_t box[4] = {64, (cuuint32_t)d->head_dim / 64, 1, (cuuint32_t)d->page_size};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1003,17 +1335,30 @@ int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const AttnArgs& ar
                 cudaStream_t stream) {
   using S = Smem<D>;
   static std::once_flag once[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
   static cudaError_t attr_err[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VAS_E_CUDA;
   std::call_once(once[dev & 63], [&] {
     attr_err[dev & 63] = cudaFuncSetAttribute(attn_bf16_kernel<D, P>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               S::kDynBytes);
   });
   if (attr_err[dev & 63] != cudaSuccess) return VAS_E_CUDA;
-  attn_bf16_kernel<D, P><<<grid, kThreads, S::kDynBytes, stream>>>(mk, mv, args);
-  return cudaGetLastError() == cudaSuccess ? VAS_OK : VAS_E_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = S::kDynBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, P>, mk, mv, args) != cudaSuccess) {
+    cudaGetLastError();
+    return VAS_E_CUDA;
+  }
+  return VAS_OK;
 }
 
 }  // namespace attn
@@ -1073,16 +1418,22 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   pa.token_seq = reinterpret_cast<int32_t*>(ws + lay.token_seq);
   pa.items = reinterpret_cast<Item*>(ws + lay.items);
   pa.header = reinterpret_cast<PlanHeader*>(ws);
+  pa.counters = reinterpret_cast<int32_t*>(ws + lay.counters);
+  pa.out = out;
+  pa.lse = lse;
   pa.B = d.num_seqs;
   pa.T = d.total_q_tokens;
   pa.G = G;
   pa.Hkv = d.num_kv_heads;
+  pa.Hq = d.num_q_heads;
+  pa.D = d.head_dim;
   pa.P = d.page_size;
   pa.maxp = d.max_pages_per_seq;
   pa.pps = kStageTokens / d.page_size;
-  pa.min_chunk = 2 * pa.pps;
+  pa.min_chunk = 4 * pa.pps;
   pa.no_split = bf16 ? 0 : 1;
   pa.target_units = kUnitsPerSm * sms;
+  pa.is_bf16 = bf16 ? 1 : 0;
   pa.items_cap = lay.items_cap;
   pa.partial_cap = lay.partial_cap;
   pa.err = err;
@@ -1098,6 +1449,7 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   aa.seqplan = pa.seqplan;
   aa.items = pa.items;
   aa.header = pa.header;
+  aa.counters = pa.counters;
   aa.part_o = reinterpret_cast<float*>(ws + lay.part_o);
   aa.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   aa.k_pages = k_pages;
@@ -1113,39 +1465,19 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   aa.scale_log2 = scale * 1.4426950408889634f;
   aa.err = err;
 
-  int rc = VAS_OK;
   if (bf16) {
     CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, k_pages, dims) || !encode_pool_map(&mv, v_pages, dims))
       return VAS_E_CUDA;
     const int grid = sms;
-    if (d.head_dim == 128 && d.page_size == 16) rc = launch_bf16<128, 16>(mk, mv, aa, grid, stream);
-    else if (d.head_dim == 128) rc = launch_bf16<128, 32>(mk, mv, aa, grid, stream);
-    else if (d.page_size == 16) rc = launch_bf16<64, 16>(mk, mv, aa, grid, stream);
-    else rc = launch_bf16<64, 32>(mk, mv, aa, grid, stream);
-  } else {
-    const int grid = 4 * sms;
-    if (d.head_dim == 128) attn_f32_kernel<128><<<grid, 128, 0, stream>>>(aa);
-    else attn_f32_kernel<64><<<grid, 128, 0, stream>>>(aa);
-    rc = cudaGetLastError() == cudaSuccess ? VAS_OK : VAS_E_CUDA;
+    if (d.head_dim == 128 && d.page_size == 16) return launch_bf16<128, 16>(mk, mv, aa, grid, stream);
+    if (d.head_dim == 128) return launch_bf16<128, 32>(mk, mv, aa, grid, stream);
+    if (d.page_size == 16) return launch_bf16<64, 16>(mk, mv, aa, grid, stream);
+    return launch_bf16<64, 32>(mk, mv, aa, grid, stream);
   }
-  if (rc != VAS_OK) return rc;
-
-  CombineArgs ca;
-  ca.seqplan = pa.seqplan;
-  ca.token_seq = pa.token_seq;
-  ca.part_o = aa.part_o;
-  ca.part_lse = aa.part_lse;
-  ca.out = out;
-  ca.lse = lse;
-  ca.T = d.total_q_tokens;
-  ca.Hq = d.num_q_heads;
-  ca.Hkv = d.num_kv_heads;
-  ca.G = G;
-  ca.D = d.head_dim;
-  ca.is_bf16 = bf16 ? 1 : 0;
-  const int64_t rows = (int64_t)d.total_q_tokens * d.num_q_heads;
-  combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(ca);
+  const int grid = 4 * sms;
+  if (d.head_dim == 128) attn_f32_kernel<128><<<grid, 128, 0, stream>>>(aa);
+  else attn_f32_kernel<64><<<grid, 128, 0, stream>>>(aa);
   return cudaGetLastError() == cudaSuccess ? VAS_OK : VAS_E_CUDA;
 }
 
