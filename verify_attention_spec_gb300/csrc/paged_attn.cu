@@ -383,15 +383,37 @@ __device__ __forceinline__ uint32_t kv_off(int t, int gc) {
   return (uint32_t)(row * 128 + (((gc & 7) ^ (row & 7)) << 4));
 }
 
+// Conditional rescaling.  Probabilities are taken against a per-row reference maximum
+// that may trail the true running maximum by up to kRebase (log2 units, so p <= 2^8);
+// the accumulators are rescaled only when a new maximum exceeds the reference by more
+// than that.  Sum and output share the reference, so the normalised result is exact.
+constexpr float kRebase = 8.f;
+
+// Per-lane ldmatrix byte offsets (relative to a stage operand) for the narrow path:
+// koff[ks]: K A-fragment of token tile 0, k-step ks; voff[dt]: V^T A-fragment of token
+// tile 0, d-tile dt.  Token tile 1 adds 16 rows.
+template <int D>
+__device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[D / 16],
+                                               uint32_t (&voff)[D / 16]) {
+  const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    koff[i] = kv_off<D>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
+    voff[i] = kv_off<D>((mi >> 1) * 8 + r8, 2 * i + (mi & 1));
+  }
+}
+
 // ---- narrow units: S^T = K Q^T, one warp per stage -------------------------------
-template <int D, int NN>
+template <int D, int NN, bool MASKED>
 __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int loaded,
                                              const uint32_t (&qb)[D / 16][NN][2],
-                                             float (&oT)[D / 16][NN][4], float (&m)[NN][2],
+                                             const uint32_t (&koff)[D / 16],
+                                             const uint32_t (&voff)[D / 16],
+                                             float (&oT)[D / 16][NN][4], float (&mref)[NN][2],
                                              float (&l)[NN][2], int t_abs0,
-                                             const int (&lim)[NN][2], bool need_mask,
-                                             float scale_log2, int lane) {
-  const int g = lane >> 2, mi = lane >> 3, r8 = lane & 7;
+                                             const int (&lim)[NN][2], float c, int lane) {
+  constexpr uint32_t kTile = 16 * D * 2;  // bytes of 16 token rows
+  const int g = lane >> 2;
   float s[2][NN][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
@@ -400,12 +422,11 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
     for (int h = 0; h < 2; ++h)
 #pragma unroll
       for (int nn = 0; nn < NN; ++nn) acc[h][nn][0] = acc[h][nn][1] = acc[h][nn][2] = acc[h][nn][3] = 0.f;
-    if (16 * mt < loaded) {
-      const int t = 16 * mt + (mi & 1) * 8 + r8;
+    if (!MASKED || 16 * mt < loaded) {
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4(kbase + kv_off<D>(t, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+        ldsm_x4(kbase + koff[ks] + mt * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(acc[ks & 1][nn], a, qb[ks][nn][0], qb[ks][nn][1]);
       }
@@ -415,77 +436,82 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
 #pragma unroll
       for (int e = 0; e < 4; ++e) s[mt][nn][e] = acc[0][nn][e] + acc[1][nn][e];
   }
+  if (MASKED) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tt = 16 * mt + g + 8 * (e >> 1);
+          if (tt >= loaded || t_abs0 + tt > lim[nn][e & 1]) s[mt][nn][e] = -INFINITY;
+        }
+  }
 
-  // Scale to log2 units, mask, running max over the stage's tokens.
+  // Rebase the rows whose maximum outgrew the reference.
   float mx[NN][2];
-#pragma unroll
-  for (int nn = 0; nn < NN; ++nn) mx[nn][0] = mx[nn][1] = -INFINITY;
-#pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nn = 0; nn < NN; ++nn)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tt = 16 * mt + g + 8 * (e >> 1);
-        const bool off = tt >= loaded || (need_mask && t_abs0 + tt > lim[nn][e & 1]);
-        const float v = off ? -INFINITY : s[mt][nn][e] * scale_log2;
-        s[mt][nn][e] = v;
-        mx[nn][e & 1] = fmaxf(mx[nn][e & 1], v);
-      }
-  float muse[NN][2], alpha[NN][2];
+  bool up = false;
 #pragma unroll
   for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float v = mx[nn][h];
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      const float mnew = fmaxf(m[nn][h], v);
-      muse[nn][h] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[nn][h] = exp2f(m[nn][h] - muse[nn][h]);
-      m[nn][h] = mnew;
+      mx[nn][h] = fmaxf(fmaxf(s[0][nn][h], s[0][nn][h + 2]), fmaxf(s[1][nn][h], s[1][nn][h + 2]));
+      up |= mx[nn][h] * c > mref[nn][h] + kRebase;
     }
+  if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+    for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float v = mx[nn][h];
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        const float vs = v * c;
+        if (vs > mref[nn][h] + kRebase) {  // same decision on all 8 lanes of the row
+          const float alpha = exp2f(mref[nn][h] - vs);
+          l[nn][h] *= alpha;
+#pragma unroll
+          for (int dt = 0; dt < D / 16; ++dt) {
+            oT[dt][nn][h] *= alpha;
+            oT[dt][nn][h + 2] *= alpha;
+          }
+          mref[nn][h] = vs;
+        }
+      }
+  }
 #pragma unroll
   for (int nn = 0; nn < NN; ++nn) {
+    const float nm0 = mref[nn][0] == -INFINITY ? 0.f : -mref[nn][0];
+    const float nm1 = mref[nn][1] == -INFINITY ? 0.f : -mref[nn][1];
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p = exp2f(s[mt][nn][e] - muse[nn][e & 1]);
+        const float p = exp2f(fmaf(s[mt][nn][e], c, (e & 1) ? nm1 : nm0));
         s[mt][nn][e] = p;
         if (e & 1) rs1 += p;
         else rs0 += p;
       }
-    l[nn][0] = l[nn][0] * alpha[nn][0] + rs0;
-    l[nn][1] = l[nn][1] * alpha[nn][1] + rs1;
+    l[nn][0] += rs0;
+    l[nn][1] += rs1;
   }
-#pragma unroll
-  for (int dt = 0; dt < D / 16; ++dt)
-#pragma unroll
-    for (int nn = 0; nn < NN; ++nn) {
-      oT[dt][nn][0] *= alpha[nn][0];
-      oT[dt][nn][1] *= alpha[nn][1];
-      oT[dt][nn][2] *= alpha[nn][0];
-      oT[dt][nn][3] *= alpha[nn][1];
-    }
 
   // O^T += V^T P^T: the P^T operand is the transpose of the S^T accumulator tile.
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    if (16 * kk < loaded) {
+    if (!MASKED || 16 * kk < loaded) {
       uint32_t pb[NN][2];
 #pragma unroll
       for (int nn = 0; nn < NN; ++nn) {
         pb[nn][0] = movmatrix_trans(pack_bf16x2(s[kk][nn][0], s[kk][nn][1]));
         pb[nn][1] = movmatrix_trans(pack_bf16x2(s[kk][nn][2], s[kk][nn][3]));
       }
-      const int t = 16 * kk + (mi >> 1) * 8 + r8;
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
         uint32_t a[4];
-        ldsm_x4_trans(vbase + kv_off<D>(t, 2 * dt + (mi & 1)), a[0], a[1], a[2], a[3]);
+        ldsm_x4_trans(vbase + voff[dt] + kk * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
       }
@@ -493,83 +519,99 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
   }
 }
 
+// Per-lane ldmatrix byte offsets for the wide path: kw[qd]: K B-fragments of token
+// tile 0 (8 rows), d-chunks 4qd..4qd+3; vw[dp]: V B-fragments of token tile 0 (16
+// rows), d-tiles 2dp, 2dp+1.
+template <int D>
+__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32],
+                                             uint32_t (&vw)[D / 16]) {
+  const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D>(r8, 4 * i + mi);
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) vw[i] = kv_off<D>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
+}
+
 // ---- wide units: S = Q K^T, warps split m16 row tiles and token slices --------------
-template <int D, int TS>
-__device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int ts0, int tvalid,
+// kbase / vbase point at this warp's token slice.
+template <int D, int TS, bool MASKED>
+__device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int tvalid,
                                            const uint32_t (&qa)[D / 16][4],
-                                           float (&o)[D / 8][4], float (&m)[2], float (&l)[2],
-                                           int t_abs0, int limA, int limB, bool need_mask,
-                                           float scale_log2, int lane) {
+                                           const uint32_t (&kw)[D / 32],
+                                           const uint32_t (&vw)[D / 16], float (&o)[D / 8][4],
+                                           float (&mref)[2], float (&l)[2], int t_abs_slice,
+                                           int limA, int limB, float c, int lane) {
   constexpr int NT = TS / 8;
-  const int tq = lane & 3, mi = lane >> 3, r8 = lane & 7;
+  const int tq = lane & 3;
   float s[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    if (8 * nt < tvalid) {
-      const int t = ts0 + 8 * nt + r8;
+    if (!MASKED || 8 * nt < tvalid) {
 #pragma unroll
       for (int qd = 0; qd < D / 32; ++qd) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + kv_off<D>(t, 4 * qd + mi), b0, b1, b2, b3);
+        ldsm_x4(kbase + kw[qd] + nt * (8 * D * 2), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
         mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
       }
     }
   }
+  if (MASKED) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tt = 8 * nt + 2 * tq + (e & 1);
+        if (tt >= tvalid || t_abs_slice + tt > ((e < 2) ? limA : limB)) s[nt][e] = -INFINITY;
+      }
+  }
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int tt = 8 * nt + 2 * tq + (e & 1);
-      const int lim = (e < 2) ? limA : limB;
-      const bool off = tt >= tvalid || (need_mask && t_abs0 + ts0 + tt > lim);
-      const float v = off ? -INFINITY : s[nt][e] * scale_log2;
-      s[nt][e] = v;
-      mx[e >> 1] = fmaxf(mx[e >> 1], v);
-    }
-  float alpha[2], muse[2];
+    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+  const bool up = mx[0] * c > mref[0] + kRebase || mx[1] * c > mref[1] + kRebase;
+  if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-    mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    const float mnew = fmaxf(m[h], mx[h]);
-    muse[h] = mnew == -INFINITY ? 0.f : mnew;
-    alpha[h] = exp2f(m[h] - muse[h]);
-    m[h] = mnew;
+    for (int h = 0; h < 2; ++h) {
+      float v = mx[h];
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+      const float vs = v * c;
+      if (vs > mref[h] + kRebase) {  // same decision on the quad sharing the row
+        const float alpha = exp2f(mref[h] - vs);
+        l[h] *= alpha;
+#pragma unroll
+        for (int dt = 0; dt < D / 8; ++dt) {
+          o[dt][2 * h] *= alpha;
+          o[dt][2 * h + 1] *= alpha;
+        }
+        mref[h] = vs;
+      }
+    }
   }
-  float rs[2] = {0.f, 0.f};
+  const float nm[2] = {mref[0] == -INFINITY ? 0.f : -mref[0], mref[1] == -INFINITY ? 0.f : -mref[1]};
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float p = exp2f(s[nt][e] - muse[e >> 1]);
+      const float p = exp2f(fmaf(s[nt][e], c, nm[e >> 1]));
       s[nt][e] = p;
-      rs[e >> 1] += p;
+      l[e >> 1] += p;
     }
-  l[0] = l[0] * alpha[0] + rs[0];
-  l[1] = l[1] * alpha[1] + rs[1];
-#pragma unroll
-  for (int dt = 0; dt < D / 8; ++dt) {
-    o[dt][0] *= alpha[0];
-    o[dt][1] *= alpha[0];
-    o[dt][2] *= alpha[1];
-    o[dt][3] *= alpha[1];
-  }
 #pragma unroll
   for (int kk = 0; kk < TS / 16; ++kk) {
-    if (16 * kk < tvalid) {
+    if (!MASKED || 16 * kk < tvalid) {
       uint32_t pa[4];
       pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
       pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
       pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-      const int t = ts0 + 16 * kk + (mi & 1) * 8 + r8;
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vbase + kv_off<D>(t, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
+        ldsm_x4_trans(vbase + vw[dp] + kk * (16 * D * 2), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dp], pa, b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
@@ -885,6 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qb[2 * kp][nn][0],
                     qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0], qb[2 * kp + 1][nn][1]);
           }
+        uint32_t koff[D / 16], voff[D / 16];
+        narrow_offsets<D>(lane, koff, voff);
         float oT[D / 16][NN][4];
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt)
@@ -926,9 +970,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
           }
-          const bool need_mask = t_abs0 + loaded - 1 > min_lim;
-          narrow_stage<D, NN>(kbase, vbase, loaded, qb, oT, m, l, t_abs0, lim, need_mask,
-                              a.scale_log2, lane);
+          if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
+            narrow_stage<D, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+                                       lim, a.scale_log2, lane);
+          else
+            narrow_stage<D, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+                                      lim, a.scale_log2, lane);
           __syncwarp();
           if (lane == 0) mbar_arrive_count(&empty[slot_s], kConsumerWarps);
         }
@@ -1019,6 +1066,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   qa[ks][2], qa[ks][3]);
         }
       }
+      uint32_t kw[D / 32], vw[D / 16];
+      wide_offsets<D>(lane, kw, vw);
       float o[D / 8][4];
 #pragma unroll
       for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
@@ -1054,13 +1103,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
             }
-            const bool need_mask = t_abs0 + ts0 + tvalid - 1 > min_lim;
-            if (TS == 16)
-              wide_stage<D, 16>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
-                                need_mask, a.scale_log2, lane);
-            else
-              wide_stage<D, 32>(kbase, vbase, ts0, tvalid, qa, o, m, l, t_abs0, limA, limB,
-                                need_mask, a.scale_log2, lane);
+            const bool interior = tvalid == TS && t_abs0 + ts0 + TS - 1 <= min_lim;
+            const uint32_t ks = kbase + ts0 * (D * 2), vs = vbase + ts0 * (D * 2);
+            const int ta = t_abs0 + ts0;
+            if (TS == 16) {
+              if (interior)
+                wide_stage<D, 16, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+              else
+                wide_stage<D, 16, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+            } else {
+              if (interior)
+                wide_stage<D, 32, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+              else
+                wide_stage<D, 32, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+            }
           }
         }
         __syncwarp();
