@@ -12,9 +12,10 @@
  *                     admission, growth, rollback of rejected drafts, eviction.
  *
  * Conventions shared by every entry point
- *  - Plain C types only.  Device pointers belong to the caller; the library allocates
- *    no device memory.  Scratch space (paged_attn_fwd's workspace) is caller-owned and
- *    sized by the matching *_workspace_size query.
+ *  - Plain C types only.  Device pointers belong to the caller and no call allocates
+ *    device memory.  Scratch space (paged_attn_fwd's workspace) is caller-owned and
+ *    sized by the matching *_workspace_size query; paged_attn_fwd_static instead uses a
+ *    fixed array the library reserves once per GPU when its device code is loaded.
  *  - Device calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  They validate their arguments on the host and return a status code
  *    immediately; nothing synchronises except vas_last_device_error.
@@ -127,6 +128,25 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* query_lens, void* out, float* lse,
                    const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
                    vas_stream_t stream);
+
+/* paged_attn_fwd without a workspace argument, for callers that cannot allocate device
+ * memory: code being captured into a CUDA graph (where cudaMalloc is not allowed), hosts
+ * that hand a plug-in only the tensors of a call, or callers whose allocator is out of
+ * memory.  The web pages have no counterpart; this is a property of the library.
+ * Scratch space is a 32 MiB array in device global memory that the library reserves on
+ * every GPU where its device code is loaded, held until the process exits; the call
+ * itself allocates nothing.  The first call on a device looks up that array's address;
+ * make that first call before any stream capture.  Arguments and results are those of
+ * paged_attn_fwd.  Returns VAS_E_WORKSPACE when the batch needs more than 32 MiB of plan
+ * space (paged_attn_workspace_min(dims) > 32 MiB; thousands of sequences fit); a batch
+ * whose split partials would not fit is split less finely instead.  Every call on a
+ * device shares the one array, and each call rewrites all of it that it reads, so no
+ * clearing is needed between calls -- but calls whose kernels may overlap on the GPU
+ * (different streams without ordering between them) race on it: order them. */
+int paged_attn_fwd_static(const void* q, const void* k_pages, const void* v_pages,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          const int32_t* query_lens, void* out, float* lse,
+                          const vas_attn_dims* dims, vas_stream_t stream);
 
 /* ==================================================================================
  * Speculative verification: modified rejection sampling
