@@ -174,7 +174,8 @@ int paged_attn_fwd_static(const void* q, const void* k_pages, const void* v_page
  * accepted_len [B]         device int32 out: j (number of accepted drafts); -1 for a
  *                          sequence with an out-of-range draft token.
  * out_tokens   [B, k+1]    device int32 out: x_0..x_{j-1}, the drawn token, then -1.
- * Rows need no alignment.  k == 0 is plain sampling from p_0.
+ * Rows need no alignment.  k == 0 is plain sampling from p_0.  k < 256 and
+ * V <= 1048576 (VAS_E_INVALID_ARG / VAS_E_UNSUPPORTED beyond).
  * Errors: VAS_E_INVALID_ARG on the host; device: VAS_DEV_BAD_TOKEN (sequence emits
  * -1s), VAS_DEV_EMPTY_ROW (position j emits -1).
  */

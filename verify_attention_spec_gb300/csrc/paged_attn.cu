@@ -177,6 +177,7 @@ __device__ __forceinline__ int32_t splits_for(const SeqShape& s, int64_t chunk) 
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
+  pdl_wait_prior_grid();    // the previous kernel in the stream has released the workspace
   pdl_launch_dependents();  // the attention grid may start its prologue
   __shared__ int32_t s_L[kPlanSmemSeqs], s_ql[kPlanSmemSeqs];
   __shared__ int64_t red[kPlanThreads / 32];
@@ -855,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       sp1 = sp2;
     }
     if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
+    pdl_launch_dependents();  // no more work for this CTA: the next kernel may launch
     // Let every copy this warp issued land before the CTA can exit.
     for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
       mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
@@ -1493,8 +1495,21 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   pa.items_cap = lay.items_cap;
   pa.partial_cap = lay.partial_cap;
   pa.err = err;
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(pa);
-  if (cudaGetLastError() != cudaSuccess) return VAS_E_CUDA;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, plan_kernel, pa) != cudaSuccess) {
+      cudaGetLastError();
+      return VAS_E_CUDA;
+    }
+  }
 
   const float scale = d.scale > 0.f ? d.scale : 1.0f / std::sqrt((float)d.head_dim);
   AttnArgs aa;

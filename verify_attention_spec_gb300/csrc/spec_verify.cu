@@ -11,11 +11,12 @@
 // vocabularies); CTA r of the cluster owns slice r of the vocabulary.  Every CTA runs
 // the k ratio tests itself (k scattered loads) and finds j.  One streaming pass over
 // its slice of row j builds w = max(0, p_j - q_j) in fp32, sums 8 contiguous elements
-// per lane in fp32 and everything above in fp64, and publishes the slice total in
-// shared memory; after a cluster barrier every CTA reads all totals through
-// distributed shared memory, so all agree on S and on the slice holding the target
-// s_j * S.  That CTA rescans its slice warp by warp (fp64 lane scans) and the crossing
-// lane walks its 8 elements.  Uniforms come from Philox4x32-10 keyed by the seed with
+// per lane in fp32 and everything above in fp64 (tile totals kept in shared memory),
+// and publishes the slice total; after a cluster barrier every CTA reads all totals
+// through distributed shared memory, so all agree on S and on the slice holding the
+// target s_j * S.  In that CTA the stored warp and tile totals locate the tile; only
+// that tile is read again, its lanes are scanned in fp64 and the crossing lane walks
+// its 8 elements.  Uniforms come from Philox4x32-10 keyed by the seed with
 // counter (position, sequence, 0, 0).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -23,6 +24,7 @@
 #include <cstdint>
 
 #include "../../include/vas.h"
+#include "device_util.cuh"
 #include "philox.cuh"
 #include "vas_internal.h"
 
@@ -37,6 +39,8 @@ constexpr int kLaneElems = 8;                  // contiguous elements per lane p
 constexpr int kTile = 32 * kLaneElems;          // elements per warp tile
 constexpr int kMaxCluster = 8;
 constexpr int kSliceMin = 4096;                 // smallest vocabulary slice per CTA
+constexpr int kMaxTilesPerWarp = 64;            // bounds the vocabulary at 8 x 8 x 64 x 256
+constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kWarps * kMaxTilesPerWarp * kTile;
 
 struct Args {
   const float* p;
@@ -95,12 +99,14 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Args a) {
 
   __shared__ int32_t s_j, s_bad;
   __shared__ double s_warp[kWarps];
+  __shared__ double s_tile[kWarps][kMaxTilesPerWarp];  // fp64 total of each warp tile
   __shared__ double s_total[2];  // this CTA's slice total, one slot per pass
   __shared__ double s_base, s_target, s_all;
   __shared__ int32_t s_owner, s_use_p, s_draw;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k = a.k, V = a.V;
+  pdl_wait_prior_grid();  // inputs written by the previous kernel in the stream are visible
   if (tid == 0) {
     s_j = k;
     s_bad = 0;
@@ -149,15 +155,35 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Args a) {
   for (int pass = 0; pass < 2; ++pass) {
     const float* qrow = use_p ? nullptr : qrow0;
     const bool vec = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
-    double acc = 0.0;
-    for (int x0 = x_begin + lane * kLaneElems; x0 < x_end; x0 += kTile) {
-      float w[kLaneElems];
-      load_weights(prow, qrow, x0, x_end, vec, w);
-      acc += (double)group_sum(w);
-    }
+    // Tile totals: fp32 over each lane's 8 elements, fp64 across the 32 lanes.  Four
+    // tiles per iteration keep several loads of each lane in flight.
+    const int n_tiles = (x_end - x_begin + kTile - 1) / kTile;
+    for (int t = 0; t < n_tiles; t += 4) {
+      float gsum[4];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) s_warp[warp] = acc;
+      for (int u = 0; u < 4; ++u) {
+        float w[kLaneElems];
+        const int x0 = x_begin + (t + u) * kTile + lane * kLaneElems;
+        if (t + u < n_tiles) load_weights(prow, qrow, x0, x_end, vec, w);
+        else
+#pragma unroll
+          for (int e = 0; e < kLaneElems; ++e) w[e] = 0.f;
+        gsum[u] = group_sum(w);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        double v = (double)gsum[u];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && t + u < n_tiles) s_tile[warp][t + u] = v;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      double acc = 0.0;
+      for (int t = 0; t < n_tiles; ++t) acc += s_tile[warp][t];
+      s_warp[warp] = acc;
+    }
     __syncthreads();
     if (tid == 0) {
       double run = 0.0;
@@ -238,9 +264,33 @@ __global__ void __launch_bounds__(kThreads) spec_verify_kernel(const Args a) {
     if (warp == s_owner) {
       const bool vec = ((reinterpret_cast<uintptr_t>(prow) | reinterpret_cast<uintptr_t>(qrow)) & 15) == 0;
       const double target = s_target;
+      // The tile that holds the target, from the stored tile totals (no memory traffic).
+      const int n_tiles = (x_end - x_begin + kTile - 1) / kTile;
       double base = s_base;
+      int t_hit = -1, t_last = -1;
+      double b_hit = 0.0, b_last = 0.0;
+      {
+        double run = base;
+        for (int t = 0; t < n_tiles; ++t) {
+          const double v = s_tile[warp][t];
+          if (v > 0.0) {
+            if (t_hit < 0 && run + v > target) {
+              t_hit = t;
+              b_hit = run;
+            }
+            t_last = t;
+            b_last = run;
+          }
+          run += v;
+        }
+      }
+      if (t_hit < 0) {
+        t_hit = t_last;
+        b_hit = b_last;
+      }
+      base = b_hit;
       int found = -1, last_pos = -1;
-      for (int t0 = x_begin; t0 < x_end && found < 0; t0 += kTile) {
+      for (int t0 = x_begin + t_hit * kTile; t0 < x_end && found < 0; t0 += kTile) {
         float w[kLaneElems];
         const int x0 = t0 + lane * kLaneElems;
         load_weights(prow, qrow, x0, x_end, vec, w);
@@ -313,6 +363,7 @@ extern "C" int spec_verify(const float* p, const float* q, const int32_t* draft_
   if ((int64_t)(k + 1) * V > INT32_MAX / 2) return VAS_E_INVALID_ARG;
   if (k >= kThreads) return VAS_E_INVALID_ARG;
   if ((int64_t)B * kMaxCluster > INT32_MAX) return VAS_E_INVALID_ARG;
+  if ((int64_t)V > kMaxVocab) return VAS_E_UNSUPPORTED;
   int32_t* err = vas::device_error_word();
   if (!err) return VAS_E_CUDA;
   int C = (V + kSliceMin - 1) / kSliceMin;
@@ -337,13 +388,15 @@ extern "C" int spec_verify(const float* p, const float* q, const int32_t* draft_
   cfg.gridDim = dim3((unsigned)(B * C));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, spec_verify_kernel, a) != cudaSuccess) {
     cudaGetLastError();
     return VAS_E_CUDA;
