@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // side); the remaining warps split the stages among themselves: a unit of <= 16
     // rows has 4 stage groups of one warp, <= 32 rows 2 groups of two, more rows one
     // group.  Each warp keeps an online softmax for its rows over its stages; the groups
-    // are merged at the end of the unit.
+    // are merged at the end of the unit, always in the same order.
     const int nRW = (Rb + 15) >> 4;
     const int n_groups = kConsumerWarps / nRW;
     const int rs = warp % nRW, sg = warp / nRW;
@@ -856,7 +856,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           lim[nn][e] = row < Rb ? L - ql + (r0 + row) / a.G : L - 1;
         }
       for (int si = 0; si < n_stages; ++si, ++stage_it) {
-        if (!active || (int)(stage_it % n_groups) != sg) continue;
+        // Ownership depends only on the unit (not on which CTA runs it), so results are
+        // identical from run to run; the unit index rotates it across short units.
+        if (!active || (si + re.u) % n_groups != sg) continue;
         const int slot_s = stage_it % kSlots;
         if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
           timed_out = true;
