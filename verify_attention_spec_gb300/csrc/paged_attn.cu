@@ -18,14 +18,15 @@
 //                       (one 4-D box per page and operand, 128-byte swizzle), tracked by
 //                       mbarriers; it prefetches the next unit's descriptor and block-
 //                       table entries while streaming.  Four consumer warps compute on
-//                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32) with
-//                       S^T = K Q^T: the KV tokens are the 16-row M side and the query
-//                       rows of the unit (GQA group x query tokens) the N side, so the 8
-//                       rows of a decode group fill an n8 tile; P^T reaches the PV operand
-//                       through movmatrix.  A warp takes 16 rows; the warps left over
-//                       split the stages (a decode unit: each warp owns every fourth
-//                       stage), each with its own online softmax, merged at the end of
-//                       the unit.
+//                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32):
+//                         narrow units (<= 16 query rows per KV head: decode, small
+//                         verify groups) take S^T = K Q^T with the KV tokens as the
+//                         16-row M side and the GQA rows as N, so 8 rows fill an n8 tile;
+//                         P^T reaches the PV operand through movmatrix.  Each warp owns
+//                         whole stages (round robin) and keeps its own online softmax;
+//                         the four are merged at the end of the unit.
+//                         wide units (17..64 rows) take S = Q K^T with the rows as M
+//                         (m16 tiles spread over the warps) and P kept in registers.
 //                       A unit covering its whole sequence writes out/lse; otherwise it
 //                       writes a normalised fp32 partial and its lse, and the last split
 //                       to finish (atomic counter, no waiting) merges them by lse:
@@ -360,7 +361,10 @@ struct Smem {
   static constexpr int kNarrowStride = D + 4;               // floats per merge row
   static constexpr int kNarrowWarpFloats = kNarrowRows * kNarrowStride + 2 * kNarrowRows;
   static constexpr int kNarrowBytes = kConsumerWarps * kNarrowWarpFloats * 4;
-  static constexpr int kScratchBytes = kQBytes > kNarrowBytes ? kQBytes : kNarrowBytes;
+  static constexpr int kWideFloats = (D / 8) * 4 + 4;       // per thread: O frags + m,l x2
+  static constexpr int kWideBytes = kConsumerWarps * 32 * kWideFloats * 4;
+  static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
+  static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
   static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
@@ -511,6 +515,106 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
         ldsm_x4_trans(vbase + voff[dt] + kk * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
+      }
+    }
+  }
+}
+
+// Per-lane ldmatrix byte offsets for the wide path: kw[qd]: K B-fragments of token
+// tile 0 (8 rows), d-chunks 4qd..4qd+3; vw[dp]: V B-fragments of token tile 0 (16
+// rows), d-tiles 2dp, 2dp+1.
+template <int D>
+__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32],
+                                             uint32_t (&vw)[D / 16]) {
+  const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D>(r8, 4 * i + mi);
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) vw[i] = kv_off<D>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
+}
+
+// ---- wide units: S = Q K^T, warps split m16 row tiles and token slices --------------
+// kbase / vbase point at this warp's token slice.
+template <int D, int TS, bool MASKED>
+__device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int tvalid,
+                                           const uint32_t (&qa)[D / 16][4],
+                                           const uint32_t (&kw)[D / 32],
+                                           const uint32_t (&vw)[D / 16], float (&o)[D / 8][4],
+                                           float (&mref)[2], float (&l)[2], int t_abs_slice,
+                                           int limA, int limB, float c, int lane) {
+  constexpr int NT = TS / 8;
+  const int tq = lane & 3;
+  float s[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    if (!MASKED || 8 * nt < tvalid) {
+#pragma unroll
+      for (int qd = 0; qd < D / 32; ++qd) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + kw[qd] + nt * (8 * D * 2), b0, b1, b2, b3);
+        mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
+        mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
+      }
+    }
+  }
+  if (MASKED) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tt = 8 * nt + 2 * tq + (e & 1);
+        if (tt >= tvalid || t_abs_slice + tt > ((e < 2) ? limA : limB)) s[nt][e] = -INFINITY;
+      }
+  }
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+  const bool up = mx[0] * c > mref[0] + kRebase || mx[1] * c > mref[1] + kRebase;
+  if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float v = mx[h];
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+      const float vs = v * c;
+      if (vs > mref[h] + kRebase) {  // same decision on the quad sharing the row
+        const float alpha = exp2f(mref[h] - vs);
+        l[h] *= alpha;
+#pragma unroll
+        for (int dt = 0; dt < D / 8; ++dt) {
+          o[dt][2 * h] *= alpha;
+          o[dt][2 * h + 1] *= alpha;
+        }
+        mref[h] = vs;
+      }
+    }
+  }
+  const float nm[2] = {mref[0] == -INFINITY ? 0.f : -mref[0], mref[1] == -INFINITY ? 0.f : -mref[1]};
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float p = exp2f(fmaf(s[nt][e], c, nm[e >> 1]));
+      s[nt][e] = p;
+      l[e >> 1] += p;
+    }
+#pragma unroll
+  for (int kk = 0; kk < TS / 16; ++kk) {
+    if (!MASKED || 16 * kk < tvalid) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(vbase + vw[dp] + kk * (16 * D * 2), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
   }
@@ -792,6 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r0 = rb * kRowBlock;
     const int Rb = min(kRowBlock, R - r0);
     const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
+    const uint32_t stage0 = stage_it;  // first stage of this unit in the CTA's stream
     const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
 
     // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
@@ -810,148 +915,131 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar_sync(1, kConsumerThreads);
 
-    // Rows are taken 16 at a time by "row warps" (K Q^T with the rows as the MMA's N
-    // side); the remaining warps split the stages among themselves: a unit of <= 16
-    // rows has 4 stage groups of one warp, <= 32 rows 2 groups of two, more rows one
-    // group.  Each warp keeps an online softmax for its rows over its stages; the groups
-    // are merged at the end of the unit, always in the same order.
-    const int nRW = (Rb + 15) >> 4;
-    const int n_groups = kConsumerWarps / nRW;
-    const int rs = warp % nRW, sg = warp / nRW;
-    const bool active = sg < n_groups;
-    const int rows_here = active ? min(16, Rb - 16 * rs) : 0;
-    // The consumers of a stage together arrive kConsumerWarps times on its empty barrier.
-    const uint32_t arrive_count = rs == 0 ? (uint32_t)(kConsumerWarps - (nRW - 1)) : 1u;
     bool poison = false;
-    auto run = [&](auto nn_tag) {
-      constexpr int NN = decltype(nn_tag)::value;
-      uint32_t qb[D / 16][NN][2];
-      if (active) {
+    if (Rb <= kNarrowRows) {
+      // ============================ narrow unit ============================
+      auto run = [&](auto nn_tag) {
+        constexpr int NN = decltype(nn_tag)::value;
+        uint32_t qb[D / 16][NN][2];
 #pragma unroll
         for (int kp = 0; kp < D / 32; ++kp)
 #pragma unroll
           for (int nn = 0; nn < NN; ++nn) {
-            const int row = 16 * rs + 8 * nn + (lane & 7);
+            const int row = 8 * nn + (lane & 7);
             const int ch = 4 * kp + (lane >> 3);
             ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qb[2 * kp][nn][0],
                     qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0], qb[2 * kp + 1][nn][1]);
           }
-      }
-      uint32_t koff[D / 16], voff[D / 16];
-      narrow_offsets<D>(lane, koff, voff);
-      float oT[D / 16][NN][4];
+        uint32_t koff[D / 16], voff[D / 16];
+        narrow_offsets<D>(lane, koff, voff);
+        float oT[D / 16][NN][4];
 #pragma unroll
-      for (int dt = 0; dt < D / 16; ++dt)
+        for (int dt = 0; dt < D / 16; ++dt)
 #pragma unroll
-        for (int nn = 0; nn < NN; ++nn) oT[dt][nn][0] = oT[dt][nn][1] = oT[dt][nn][2] = oT[dt][nn][3] = 0.f;
-      float m[NN][2], l[NN][2];
-      int lim[NN][2];
-#pragma unroll
-      for (int nn = 0; nn < NN; ++nn)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          m[nn][e] = -INFINITY;
-          l[nn][e] = 0.f;
-          const int row = 16 * rs + 8 * nn + 2 * tq + e;
-          lim[nn][e] = row < Rb ? L - ql + (r0 + row) / a.G : L - 1;
-        }
-      for (int si = 0; si < n_stages; ++si, ++stage_it) {
-        // Ownership depends only on the unit (not on which CTA runs it), so results are
-        // identical from run to run; the unit index rotates it across short units.
-        if (!active || (si + re.u) % n_groups != sg) continue;
-        const int slot_s = stage_it % kSlots;
-        if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
-          timed_out = true;
-          stage_it += n_stages - si;
-          break;
-        }
-        if (meta[slot_s]) poison = true;
-        const int pg = it.page_begin + si * PPS;
-        const int loaded = min(PPS, it.page_end - pg) * P;
-        const int t_abs0 = pg * P;
-        const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
-        const uint32_t vbase = kbase + S::kOperandBytes;
-        if (t_abs0 + loaded > L) {
-          // Pool slots past the end of the sequence may hold anything: zero their V
-          // rows so that a zero attention weight cannot meet a NaN.  Several warps may
-          // read a stage; each zeroes before its own reads (all write the same zeros).
-          uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
-          const int z0 = max(0, L - t_abs0);
-          for (int c = z0 * (D / 8) + lane; c < loaded * (D / 8); c += 32)
-            *reinterpret_cast<uint4*>(vrow + kv_off<D>(c / (D / 8), c % (D / 8))) =
-                make_uint4(0, 0, 0, 0);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
-          narrow_stage<D, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                     lim, a.scale_log2, lane);
-        else
-          narrow_stage<D, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                    lim, a.scale_log2, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_count(&empty[slot_s], arrive_count);
-      }
-#pragma unroll
-      for (int nn = 0; nn < NN; ++nn)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 4);
-          l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 8);
-          l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 16);
-        }
-      // Stash this warp's state for the merge (the scratch held the query rows).
-      named_bar_sync(1, kConsumerThreads);
-      float* wb = reinterpret_cast<float*>(scratch) + (size_t)warp * S::kNarrowWarpFloats;
-#pragma unroll
-      for (int dt = 0; dt < D / 16; ++dt)
-#pragma unroll
-        for (int nn = 0; nn < NN; ++nn)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            wb[(8 * nn + 2 * tq + (e & 1)) * S::kNarrowStride + 16 * dt + g + 8 * (e >> 1)] =
-                oT[dt][nn][e];
-      if (g == 0)
+          for (int nn = 0; nn < NN; ++nn) oT[dt][nn][0] = oT[dt][nn][1] = oT[dt][nn][2] = oT[dt][nn][3] = 0.f;
+        float m[NN][2], l[NN][2];
+        int lim[NN][2];
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            wb[kNarrowRows * S::kNarrowStride + 8 * nn + 2 * tq + e] = m[nn][e];
-            wb[kNarrowRows * S::kNarrowStride + kNarrowRows + 8 * nn + 2 * tq + e] = l[nn][e];
+            m[nn][e] = -INFINITY;
+            l[nn][e] = 0.f;
+            const int row = 8 * nn + 2 * tq + e;
+            lim[nn][e] = row < Rb ? L - ql + (r0 + row) / a.G : L - 1;
           }
-    };
-    if (rows_here > 8) run(std::integral_constant<int, 2>{});
-    else run(std::integral_constant<int, 1>{});
-    // Bad pages and timeouts seen by any warp concern the whole unit.
-    poison = named_bar_or(1, kConsumerThreads, poison);
-    if (named_bar_or(1, kConsumerThreads, timed_out)) {
-      timed_out = true;
-      break;
-    }
-    {
+        for (int si = 0; si < n_stages; ++si, ++stage_it) {
+          if ((int)(stage_it % kConsumerWarps) != warp) continue;
+          const int slot_s = stage_it % kSlots;
+          if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+            timed_out = true;
+            stage_it += n_stages - si;
+            break;
+          }
+          if (meta[slot_s]) poison = true;
+          const int pg = it.page_begin + si * PPS;
+          const int loaded = min(PPS, it.page_end - pg) * P;
+          const int t_abs0 = pg * P;
+          const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
+          const uint32_t vbase = kbase + S::kOperandBytes;
+          if (t_abs0 + loaded > L) {
+            // Pool slots past the end of the sequence may hold anything: zero their V
+            // rows so that a zero attention weight cannot meet a NaN.
+            uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+            const int z0 = max(0, L - t_abs0);
+            for (int c = z0 * (D / 8) + lane; c < loaded * (D / 8); c += 32)
+              *reinterpret_cast<uint4*>(vrow + kv_off<D>(c / (D / 8), c % (D / 8))) =
+                  make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
+            narrow_stage<D, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+                                       lim, a.scale_log2, lane);
+          else
+            narrow_stage<D, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+                                      lim, a.scale_log2, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive_count(&empty[slot_s], kConsumerWarps);
+        }
+#pragma unroll
+        for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 4);
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 8);
+            l[nn][e] += __shfl_xor_sync(0xffffffffu, l[nn][e], 16);
+          }
+        // Merge the four warps' states through shared memory.
+        named_bar_sync(1, kConsumerThreads);  // all warps are done with the Q rows
+        float* wb = reinterpret_cast<float*>(scratch) + (size_t)warp * S::kNarrowWarpFloats;
+        // Rows a warp never touched keep m = -inf, l = 0 and contribute nothing.
+#pragma unroll
+        for (int dt = 0; dt < D / 16; ++dt)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              wb[(8 * nn + 2 * tq + (e & 1)) * S::kNarrowStride + 16 * dt + g + 8 * (e >> 1)] =
+                  oT[dt][nn][e];
+        if (g == 0)
+#pragma unroll
+          for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              wb[kNarrowRows * S::kNarrowStride + 8 * nn + 2 * tq + e] = m[nn][e];
+              wb[kNarrowRows * S::kNarrowStride + kNarrowRows + 8 * nn + 2 * tq + e] = l[nn][e];
+            }
+      };
+      if (Rb <= 8) run(std::integral_constant<int, 1>{});
+      else run(std::integral_constant<int, 2>{});
+      // Bad pages and timeouts seen by any warp's stages concern the whole unit.
+      poison = named_bar_or(1, kConsumerThreads, poison);
+      if (named_bar_or(1, kConsumerThreads, timed_out)) {
+        timed_out = true;
+        break;
+      }
       const float* buf = reinterpret_cast<const float*>(scratch);
       const int d = warp * 32 + lane;  // this lane's output column
+      // Warp w took the stages with (stage0 + si) % 4 == w.  Summing the partitions in
+      // the order of si % 4, not of w, makes the result independent of stage0, i.e. of
+      // which units this CTA happened to run before: reruns are bit-identical.
       for (int r = 0; r < Rb; ++r) {
-        const int rsr = r >> 4, lr = r & 15;
         float mw[kConsumerWarps], M = -INFINITY;
 #pragma unroll
-        for (int gi = 0; gi < kConsumerWarps; ++gi) {
-          mw[gi] = -INFINITY;
-          if (gi < n_groups) {
-            mw[gi] = buf[(rsr + nRW * gi) * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + lr];
-            M = fmaxf(M, mw[gi]);
-          }
+        for (int pt = 0; pt < kConsumerWarps; ++pt) {
+          const int w = (stage0 + pt) % kConsumerWarps;
+          mw[pt] = buf[w * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + r];
+          M = fmaxf(M, mw[pt]);
         }
         const float mu = M == -INFINITY ? 0.f : M;
         float Lsum = 0.f, acc = 0.f;
 #pragma unroll
-        for (int gi = 0; gi < kConsumerWarps; ++gi) {
-          if (gi < n_groups) {
-            const float* wbuf = buf + (rsr + nRW * gi) * S::kNarrowWarpFloats;
-            const float f = exp2f(mw[gi] - mu);
-            Lsum += f * wbuf[kNarrowRows * S::kNarrowStride + kNarrowRows + lr];
-            if (d < D) acc += f * wbuf[lr * S::kNarrowStride + d];
-          }
+        for (int pt = 0; pt < kConsumerWarps; ++pt) {
+          const int w = (stage0 + pt) % kConsumerWarps;
+          const float f = exp2f(mw[pt] - mu);
+          Lsum += f * buf[w * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + kNarrowRows + r];
+          if (d < D) acc += f * buf[w * S::kNarrowWarpFloats + r * S::kNarrowStride + d];
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
         float row_lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
@@ -965,6 +1053,155 @@ __global__ void __launch_bounds__(kThreads, 1)
           const size_t prow = partial_row(a, sp, split, head, r0 + r);
           if (d < D) a.part_o[prow * D + d] = x;
           if (warp == 0 && lane == 0) a.part_lse[prow] = row_lse;
+        }
+      }
+    } else {
+      // ============================= wide unit =============================
+      const int nM = (Rb + 15) >> 4;
+      const int nW = nM == 2 ? 2 : 1;
+      const bool active = warp < nM * nW;
+      const int mt = warp % nM;
+      const int slice = warp / nM;
+      const int TS = kStageTokens / nW;
+      uint32_t qa[D / 16][4];
+      if (active) {
+        const int mi = lane >> 3;
+        const int row = 16 * mt + (mi & 1) * 8 + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int ch = 2 * ks + (mi >> 1);
+          ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qa[ks][0], qa[ks][1],
+                  qa[ks][2], qa[ks][3]);
+        }
+      }
+      uint32_t kw[D / 32], vw[D / 16];
+      wide_offsets<D>(lane, kw, vw);
+      float o[D / 8][4];
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      const int rA = r0 + 16 * mt + g, rB = rA + 8;
+      const int limA = rA < R ? L - ql + rA / a.G : L - 1;
+      const int limB = rB < R ? L - ql + rB / a.G : L - 1;
+      for (int si = 0; si < n_stages; ++si, ++stage_it) {
+        const int slot_s = stage_it % kSlots;
+        if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+          timed_out = true;
+          stage_it += n_stages - si;
+          break;
+        }
+        if (meta[slot_s]) poison = true;
+        const int pg = it.page_begin + si * PPS;
+        const int loaded = min(PPS, it.page_end - pg) * P;
+        const int t_abs0 = pg * P;
+        const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
+        const uint32_t vbase = kbase + S::kOperandBytes;
+        if (active) {
+          const int ts0 = slice * TS;
+          const int tvalid = min(TS, loaded - ts0);
+          if (tvalid > 0) {
+            if (t_abs0 + ts0 + tvalid > L) {
+              // Several warps read these rows: each zeroes them before its own reads
+              // (all write the same zeros).
+              uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+              const int z0 = max(0, L - t_abs0 - ts0);
+              for (int c = z0 * (D / 8) + lane; c < tvalid * (D / 8); c += 32)
+                *reinterpret_cast<uint4*>(vrow + kv_off<D>(ts0 + c / (D / 8), c % (D / 8))) =
+                    make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+              __syncwarp();
+            }
+            const bool interior = tvalid == TS && t_abs0 + ts0 + TS - 1 <= min_lim;
+            const uint32_t ks = kbase + ts0 * (D * 2), vs = vbase + ts0 * (D * 2);
+            const int ta = t_abs0 + ts0;
+            if (TS == 16) {
+              if (interior)
+                wide_stage<D, 16, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+              else
+                wide_stage<D, 16, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+            } else {
+              if (interior)
+                wide_stage<D, 32, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+              else
+                wide_stage<D, 32, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot_s]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+      }
+      float* cb = reinterpret_cast<float*>(scratch);
+      named_bar_sync(1, kConsumerThreads);  // everyone is done with the Q rows
+      if (active && nW > 1 && slice > 0) {
+        float* mine = cb + (size_t)warp * 32 * S::kWideFloats;
+#pragma unroll
+        for (int dt = 0; dt < D / 8; ++dt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mine[(dt * 4 + e) * 32 + lane] = o[dt][e];
+        mine[(D / 2 + 0) * 32 + lane] = m[0];
+        mine[(D / 2 + 1) * 32 + lane] = m[1];
+        mine[(D / 2 + 2) * 32 + lane] = l[0];
+        mine[(D / 2 + 3) * 32 + lane] = l[1];
+      }
+      poison = named_bar_or(1, kConsumerThreads, poison);
+      if (named_bar_or(1, kConsumerThreads, timed_out)) {
+        timed_out = true;
+        break;
+      }
+      if (active && slice == 0) {
+        for (int sl = 1; sl < nW; ++sl) {
+          const float* other = cb + (size_t)(mt + sl * nM) * 32 * S::kWideFloats;
+          const float om[2] = {other[(D / 2 + 0) * 32 + lane], other[(D / 2 + 1) * 32 + lane]};
+          const float ol[2] = {other[(D / 2 + 2) * 32 + lane], other[(D / 2 + 3) * 32 + lane]};
+          float fa[2], fb[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float mm = fmaxf(m[h], om[h]);
+            const float mu = mm == -INFINITY ? 0.f : mm;
+            fa[h] = exp2f(m[h] - mu);
+            fb[h] = exp2f(om[h] - mu);
+            l[h] = l[h] * fa[h] + ol[h] * fb[h];
+            m[h] = mm;
+          }
+#pragma unroll
+          for (int dt = 0; dt < D / 8; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              o[dt][e] = o[dt][e] * fa[e >> 1] + other[(dt * 4 + e) * 32 + lane] * fb[e >> 1];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = h ? rB : rA;
+          if (r >= r0 + Rb) continue;
+          const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+          float row_lse = l[h] > 0.f ? (m[h] + log2f(l[h])) * kLn2 : -INFINITY;
+          if (poison) row_lse = NAN;
+          if (sp.nsplit == 1) {
+            const size_t orow = out_row(a, sp, head, r);
+            __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + orow * D;
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) {
+              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
+              if (poison) x0 = x1 = NAN;
+              *reinterpret_cast<uint32_t*>(og + dt * 8 + 2 * tq) = pack_bf16x2(x0, x1);
+            }
+            if (tq == 0) a.lse[orow] = row_lse;
+          } else {
+            const size_t prow = partial_row(a, sp, split, head, r);
+            float* po = a.part_o + prow * D;
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) {
+              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
+              if (poison) x0 = x1 = NAN;
+              *reinterpret_cast<float2*>(po + dt * 8 + 2 * tq) = make_float2(x0, x1);
+            }
+            if (tq == 0) a.part_lse[prow] = row_lse;
+          }
         }
       }
     }
