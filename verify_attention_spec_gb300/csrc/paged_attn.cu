@@ -14,7 +14,7 @@
 //   2. attn_bf16_kernel persistent, one CTA per SM, launched as a programmatic
 //                       dependent of the plan.  A producer warp takes work units (work
 //                       item x KV head) from an atomic counter and streams the unit's
-//                       K/V page slices into an 8-slot ring of 32-token stages with TMA
+//                       K/V page slices into an 11-slot ring of 32-token stages with TMA
 //                       (one 4-D box per page and operand, 128-byte swizzle), tracked by
 //                       mbarriers; it prefetches the next unit's descriptor and block-
 //                       table entries while streaming.  Four consumer warps compute on
@@ -53,7 +53,7 @@ namespace vas {
 namespace attn {
 
 constexpr int kStageTokens = 32;   // KV tokens per pipeline stage
-constexpr int kSlots = 8;          // stages in the shared-memory ring
+constexpr int kSlots = 11;         // stages in the shared-memory ring
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
@@ -121,40 +121,6 @@ struct PlanArgs {
   int32_t* err;
 };
 
-__device__ __forceinline__ int64_t block_sum_i64(int64_t v, int64_t* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  int64_t t = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
-  return t;
-}
-
-// Exclusive scan of v over the block (threads in order); *total gets the block total.
-__device__ __forceinline__ int64_t block_excl_scan_i64(int64_t v, int64_t* red,
-                                                       int64_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  __syncthreads();
-  if (lane == 31) red[warp] = inc;
-  __syncthreads();
-  int64_t before = 0, all = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) before += red[w];
-    all += red[w];
-  }
-  *total = all;
-  return before + inc - v;
-}
-
 struct SeqShape {
   bool valid;
   int32_t L, ql, npages, R, nrb;
@@ -176,16 +142,77 @@ __device__ __forceinline__ int32_t splits_for(const SeqShape& s, int64_t chunk) 
   return (int32_t)((s.npages + chunk - 1) / chunk);
 }
 
+// Block-wide sums of three counters at once.
+__device__ __forceinline__ void block_sum3(int64_t& x, int64_t& y, int64_t& z, int64_t (*red)[3]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    x += __shfl_xor_sync(0xffffffffu, x, o);
+    y += __shfl_xor_sync(0xffffffffu, y, o);
+    z += __shfl_xor_sync(0xffffffffu, z, o);
+  }
+  __syncthreads();
+  if (lane == 0) {
+    red[warp][0] = x;
+    red[warp][1] = y;
+    red[warp][2] = z;
+  }
+  __syncthreads();
+  x = y = z = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    x += red[w][0];
+    y += red[w][1];
+    z += red[w][2];
+  }
+}
+
+// Exclusive scans of three counters at once (threads in order); totals returned in t*.
+__device__ __forceinline__ void block_scan3(int64_t& x, int64_t& y, int64_t& z, int64_t (*red)[3],
+                                            int64_t& tx, int64_t& ty, int64_t& tz) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t ix = x, iy = y, iz = z;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t nx = __shfl_up_sync(0xffffffffu, ix, o);
+    const int64_t ny = __shfl_up_sync(0xffffffffu, iy, o);
+    const int64_t nz = __shfl_up_sync(0xffffffffu, iz, o);
+    if (lane >= o) {
+      ix += nx;
+      iy += ny;
+      iz += nz;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) {
+    red[warp][0] = ix;
+    red[warp][1] = iy;
+    red[warp][2] = iz;
+  }
+  __syncthreads();
+  int64_t bx = 0, by = 0, bz = 0;
+  tx = ty = tz = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+    if (w < warp) {
+      bx += red[w][0];
+      by += red[w][1];
+      bz += red[w][2];
+    }
+    tx += red[w][0];
+    ty += red[w][1];
+    tz += red[w][2];
+  }
+  x = bx + ix - x;
+  y = by + iy - y;
+  z = bz + iz - z;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   pdl_wait_prior_grid();    // the previous kernel in the stream has released the workspace
   pdl_launch_dependents();  // the attention grid may start its prologue
   __shared__ int32_t s_L[kPlanSmemSeqs], s_ql[kPlanSmemSeqs];
-  __shared__ int64_t red[kPlanThreads / 32];
-  __shared__ int64_t s_chunk;
-  __shared__ int32_t s_bad;
+  __shared__ int64_t red[kPlanThreads / 32][3];
   const int tid = threadIdx.x;
   const bool cached = a.B <= kPlanSmemSeqs;
-  if (tid == 0) s_bad = 0;
   if (cached)
     for (int i = tid; i < a.B; i += kPlanThreads) {
       s_L[i] = a.seq_lens[i];
@@ -196,51 +223,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     return cached ? seq_shape(a, s_L[i], s_ql[i]) : seq_shape(a, a.seq_lens[i], a.query_lens[i]);
   };
 
-  // Totals: work in page-row-blocks per KV head, and the packed query rows.
-  int64_t cost = 0, rows = 0;
+  // Totals: work in page-row-blocks per KV head, packed query rows, invalid sequences.
+  int64_t cost = 0, rows = 0, bad = 0;
   for (int i = tid; i < a.B; i += kPlanThreads) {
     const SeqShape s = shape(i);
-    if (!s.valid) s_bad = 1;
+    bad += !s.valid;
     cost += (int64_t)s.npages * s.nrb;
     rows += s.ql > 0 ? s.ql : 0;
   }
-  const int64_t total_cost = block_sum_i64(cost, red);
-  const int64_t total_rows = block_sum_i64(rows, red);
-  if (tid == 0 && (total_rows != a.T || s_bad)) atomicOr(a.err, VAS_DEV_BAD_LENGTHS);
+  block_sum3(cost, rows, bad, red);
+  const bool lengths_ok = rows == a.T && bad == 0;
+  if (tid == 0 && !lengths_ok) atomicOr(a.err, VAS_DEV_BAD_LENGTHS);
 
   // Split length: about kUnitsPerSm units per SM, at least min_chunk pages, a whole
   // number of stages; doubled until the work list and the partials fit the workspace.
-  if (tid == 0) {
-    int64_t c;
-    if (a.no_split) {
-      c = INT_MAX;
-    } else {
-      const int64_t want = (total_cost * a.Hkv + a.target_units - 1) / a.target_units;
-      c = want > a.min_chunk ? want : a.min_chunk;
-      c = (c + a.pps - 1) / a.pps * a.pps;
-    }
-    s_chunk = c;
+  int64_t c;
+  if (a.no_split) {
+    c = INT_MAX;
+  } else {
+    const int64_t want = (cost * a.Hkv + a.target_units - 1) / a.target_units;
+    c = want > a.min_chunk ? want : a.min_chunk;
+    c = (c + a.pps - 1) / a.pps * a.pps;
   }
-  __syncthreads();
   for (int iter = 0; iter < 40; ++iter) {
-    const int64_t c = s_chunk;
-    int64_t n_items = 0, n_part = 0;
+    int64_t n_items = 0, n_part = 0, unused = 0;
     for (int i = tid; i < a.B; i += kPlanThreads) {
       const SeqShape s = shape(i);
       const int32_t ns = splits_for(s, c);
       n_items += (int64_t)ns * s.nrb;
       if (ns > 1) n_part += (int64_t)ns * a.Hkv * s.R;
     }
-    const int64_t tot_items = block_sum_i64(n_items, red);
-    const int64_t tot_part = block_sum_i64(n_part, red);
-    __syncthreads();
-    if ((tot_items <= a.items_cap && tot_part <= a.partial_cap) || c >= INT_MAX / 2) break;
-    if (tid == 0) s_chunk = c * 2 < INT_MAX ? c * 2 : INT_MAX;
-    __syncthreads();
+    block_sum3(n_items, n_part, unused, red);
+    if ((n_items <= a.items_cap && n_part <= a.partial_cap) || c >= INT_MAX / 2) break;
+    c = c * 2 < INT_MAX ? c * 2 : INT_MAX;
   }
-  const int64_t c = s_chunk;
-
-  for (int r = tid; r < a.T; r += kPlanThreads) a.token_seq[r] = -1;
+  if (!lengths_ok)  // the row -> sequence map is only needed to find rows to NaN-fill
+    for (int r = tid; r < a.T; r += kPlanThreads) a.token_seq[r] = -1;
   __syncthreads();
 
   // Scans in batch order, kPlanThreads sequences at a time.
@@ -256,11 +274,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       qrows = s.ql > 0 ? s.ql : 0;
       ns = splits_for(s, c);
     }
+    int64_t my_row0 = qrows, my_item0 = (int64_t)ns * s.nrb;
+    int64_t my_part0 = ns > 1 ? (int64_t)ns * a.Hkv * s.R : 0;
     int64_t t_rows, t_items, t_part;
-    const int64_t my_row0 = carry_rows + block_excl_scan_i64(qrows, red, &t_rows);
-    const int64_t my_item0 = carry_items + block_excl_scan_i64((int64_t)ns * s.nrb, red, &t_items);
-    const int64_t my_part0 =
-        carry_part + block_excl_scan_i64(ns > 1 ? (int64_t)ns * a.Hkv * s.R : 0, red, &t_part);
+    block_scan3(my_row0, my_item0, my_part0, red, t_rows, t_items, t_part);
+    my_row0 += carry_rows;
+    my_item0 += carry_items;
+    my_part0 += carry_part;
     if (i < a.B) {
       SeqPlan sp;
       sp.qrow0 = (int32_t)my_row0;
@@ -278,7 +298,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       sp.partial_base = (int32_t)my_part0;
       sp.item0 = (int32_t)(my_item0 < a.items_cap ? my_item0 : 0);
       a.seqplan[i] = sp;
-      for (int j = 0; j < qrows && my_row0 + j < a.T; ++j) a.token_seq[my_row0 + j] = i;
+      if (!lengths_ok)
+        for (int j = 0; j < qrows && my_row0 + j < a.T; ++j) a.token_seq[my_row0 + j] = i;
       if (ns > 0) {
         // A skipped sequence keeps its slots below the capacity as null items.
         int64_t it = my_item0;
@@ -308,6 +329,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     a.header->chunk_pages = (int32_t)(c < INT_MAX ? c : INT_MAX);
     a.header->n_partial_rows = (int32_t)carry_part;
   }
+  if (lengths_ok) return;
   __syncthreads();
 
   // Rows owned by no sequence, or by one with inconsistent lengths, are NaN.
@@ -684,23 +706,41 @@ __device__ void merge_splits(const AttnArgs& a, const SeqPlan& sp, int head, int
   }
 }
 
-// After this CTA wrote its partial rows: count the arrival; the last split merges.
-template <int D>
-__device__ __forceinline__ void finish_split(const AttnArgs& a, const SeqPlan& sp,
-                                             const Item& it, int head, int r0, int Rb,
-                                             int32_t* flag, int warp, int lane) {
-  __threadfence();
-  named_bar_sync(1, kConsumerThreads);
+// A split unit whose arrival was counted; the CTA that counted last merges the rows.
+// The count's result is only examined at the start of the CTA's next unit, so the
+// atomic's round trip overlaps the hand-over to that unit.
+struct PendingMerge {
+  SeqPlan sp;
+  int32_t head, r0, Rb, valid;
+  int32_t old;  // thread 0 only: the counter's value before this CTA's arrival
+};
+
+// All consumer threads: the CTA's partial rows have been written.
+__device__ __forceinline__ void count_split_arrival(const AttnArgs& a, const SeqPlan& sp,
+                                                    const Item& it, int head, int r0, int Rb,
+                                                    PendingMerge& pm) {
+  named_bar_sync(1, kConsumerThreads);  // every partial store of the CTA is issued
   if (threadIdx.x == 0) {
     const int rb = it.split_rb & ((1 << kRbBits) - 1);
-    int32_t* cnt = a.counters + ((size_t)sp.item0 + rb) * a.Hkv + head;
-    *flag = atomicAdd(cnt, 1) == sp.nsplit - 1;
+    __threadfence();  // orders the CTA's partials before the count (cumulative via the barrier)
+    pm.old = atomicAdd(a.counters + ((size_t)sp.item0 + rb) * a.Hkv + head, 1);
   }
-  named_bar_sync(1, kConsumerThreads);
-  if (*flag) {
+  pm.sp = sp;
+  pm.head = head;
+  pm.r0 = r0;
+  pm.Rb = Rb;
+  pm.valid = 1;
+}
+
+// All consumer threads; `flag` was set by thread 0 before the last named barrier.
+template <int D>
+__device__ __forceinline__ void finish_pending(const AttnArgs& a, PendingMerge& pm,
+                                               const int32_t* flag, int warp, int lane) {
+  if (pm.valid && *flag) {
     __threadfence();
-    merge_splits<D>(a, sp, head, r0, Rb, warp, lane);
+    merge_splits<D>(a, pm.sp, pm.head, pm.r0, pm.Rb, warp, lane);
   }
+  pm.valid = 0;
 }
 
 template <int D, int P>
@@ -869,9 +909,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float kLn2 = 0.6931471805599453f;
   uint32_t stage_it = 0, unit_it = 0;
   bool timed_out = false;
+  PendingMerge pm;
+  pm.valid = 0;
+  pm.old = 0;
   for (;;) {
     const int slot = unit_it % kRing;
     const bool got = mbar_wait(&ufull[slot], (unit_it / kRing) & 1);
+    if (tid == 0) *flag = pm.valid && pm.old == pm.sp.nsplit - 1;
     RingEntry re;
     re.u = -1;
     if (got) re = ring[slot];
@@ -881,7 +925,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every consumer warp takes the same decision (a warp that left alone would strand
     // the others at a named barrier); this barrier also frees the scratch area of the
     // previous unit's merge for the next query rows.
-    if (named_bar_or(1, kConsumerThreads, !got)) {
+    const bool stop = named_bar_or(1, kConsumerThreads, !got);
+    finish_pending<D>(a, pm, flag, warp, lane);  // the previous unit's merge, if this CTA was last
+    if (stop) {
       timed_out = true;
       break;
     }
@@ -1206,7 +1252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (poison && tid == 0) atomicOr(a.err, VAS_DEV_BAD_PAGE);
-    if (sp.nsplit > 1) finish_split<D>(a, sp, it, head, r0, Rb, flag, warp, lane);
+    if (sp.nsplit > 1) count_split_arrival(a, sp, it, head, r0, Rb, pm);
   }
   if (timed_out && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
 }
