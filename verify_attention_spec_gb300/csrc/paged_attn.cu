@@ -14,7 +14,7 @@
 //   2. attn_bf16_kernel persistent, one CTA per SM, launched as a programmatic
 //                       dependent of the plan.  A producer warp takes work units (work
 //                       item x KV head) from an atomic counter and streams the unit's
-//                       K/V page slices into an 11-slot ring of 32-token stages with TMA
+//                       K/V page slices into an 8-slot ring of 32-token stages with TMA
 //                       (one 4-D box per page and operand, 128-byte swizzle), tracked by
 //                       mbarriers; it prefetches the next unit's descriptor and block-
 //                       table entries while streaming.  Four consumer warps compute on
@@ -53,11 +53,17 @@ namespace vas {
 namespace attn {
 
 constexpr int kStageTokens = 32;   // KV tokens per pipeline stage
-constexpr int kSlots = 11;         // stages in the shared-memory ring
+constexpr int kSlots = 8;          // stages in the shared-memory ring
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
 constexpr int kRowBlock = 64;      // query rows per unit (four m16 tiles)
+// In a decode unit warp w consumes the stages s with s % kConsumerWarps == w and waits
+// on slot s % kSlots by phase parity.  The parity test is only sound if the slot's
+// previous fill was consumed by the same warp, i.e. if kSlots is a multiple of the
+// number of consumer warps; otherwise a warp could pass the parity test while the
+// slot's previous fill is still in flight.
+static_assert(kSlots % kConsumerWarps == 0, "stage slots must be a multiple of the consumer warps");
 constexpr int kNarrowRows = 16;    // units with at most this many rows take the K Q^T form
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
