@@ -186,3 +186,14 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool
 }
 
 }  // namespace vas
+
+namespace vas {
+
+// L2 policy for data re-read by later work of the same call.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+}  // namespace vas
