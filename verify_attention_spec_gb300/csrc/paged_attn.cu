@@ -667,6 +667,21 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
   }
 }
 
+// Whether the producer brings this unit's query rows into its ring buffer by TMA (the
+// same test on both sides): a row block of <= kNarrowRows rows made of whole query
+// tokens.  *j0 / *nj: its first query token and token count.
+__device__ __forceinline__ bool unit_q_in_ring(const AttnArgs& a, const Item& it,
+                                               const SeqPlan& sp, int* j0, int* nj) {
+  if (!a.q_tma || it.seq < 0) return false;
+  const int R = a.G * sp.qlen;
+  const int r0 = (it.split_rb & ((1 << kRbBits) - 1)) * kRowBlock;
+  const int Rb = min(kRowBlock, R - r0);
+  if (Rb > kNarrowRows || r0 % a.G != 0 || Rb % a.G != 0) return false;
+  *j0 = r0 / a.G;
+  *nj = Rb / a.G;
+  return true;
+}
+
 // ---- output helpers ----------------------------------------------------------------
 __device__ __forceinline__ size_t out_row(const AttnArgs& a, const SeqPlan& sp, int head, int r) {
   const int j = r / a.G, hh = r % a.G;
@@ -860,15 +875,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         e.sp = sp;
         e.pad[0] = e.pad[1] = 0;
         ring[slot] = e;
-        const int R = a.G * sp.qlen;
-        if (a.q_tma && it.seq >= 0 && R <= kNarrowRows) {
-          // A decode-like unit (one row block): its query rows, token by token, land in
-          // this ring slot's buffer; the consumers' wait on ufull covers them.
-          mbar_arrive_expect_tx(&ufull[slot], (uint32_t)(R * D * 2));
+        int j0 = 0, nj = 0;
+        if (unit_q_in_ring(a, it, sp, &j0, &nj)) {
+          // A narrow row block: its query rows, token by token, land in this ring slot's
+          // buffer; the consumers' wait on ufull covers them.
+          mbar_arrive_expect_tx(&ufull[slot], (uint32_t)(nj * a.G * D * 2));
           uint8_t* qdst = qring + slot * S::kQBufBytes;
-          for (int j = 0; j < sp.qlen; ++j)
+          for (int j = 0; j < nj; ++j)
             tma_load_4d(qdst + j * a.G * D * 2, &tm_q, &ufull[slot], 0, 0, (u % a.Hkv) * a.G,
-                        sp.qrow0 + j, pol_q);
+                        sp.qrow0 + j0 + j, pol_q);
         } else {
           mbar_arrive(&ufull[slot]);
         }
@@ -989,7 +1004,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Query rows (row r: token r / G, head head * G + r % G).  A unit the producer
     // brought them for reads them from its ring buffer; otherwise they are staged here,
     // rows past Rb up to the MMA tile zero.
-    const bool q_in_ring = a.q_tma && Rb <= kNarrowRows;
+    int qj0, qnj;
+    const bool q_in_ring = unit_q_in_ring(a, it, sp, &qj0, &qnj);
     const uint8_t* qbuf = qring + slot * S::kQBufBytes;
     if (!q_in_ring) {
       constexpr int kChunks = D / 8;
