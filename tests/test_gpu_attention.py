@@ -50,7 +50,8 @@ def _case(lens, qlens, Hq=8, Hkv=2, D=128, P=16, dtype=wl.BF16, seed=3, pool_pag
 
 
 @pytest.mark.parametrize("D,P,Hq,Hkv", [(128, 16, 8, 2), (128, 32, 64, 8), (64, 16, 4, 4),
-                                        (64, 32, 16, 2)])
+                                        (64, 32, 16, 2), (128, 16, 4, 2), (128, 32, 64, 2),
+                                        (128, 16, 8, 8)])
 @pytest.mark.parametrize("dtype", [wl.BF16, wl.F32])
 def test_shapes_and_ragged_edges(vas_lib, D, P, Hq, Hkv, dtype):
     """Page boundaries (L = P, P+1), a single token, a window covering the whole context
