@@ -1679,9 +1679,8 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
     // The query map brings a decode unit's G rows of one token as one box; it is used
     // when G <= 16 and each token's rows start on a 1024-byte boundary of the buffer,
     // where the 128-byte swizzle pattern restarts.
-    // Otherwise the kernel never reads the query map, but the launch still wants a valid
-    // one in that parameter (a zeroed map is refused as an invalid argument): it gets the
-    // K map.
+    // Otherwise the kernel never reads the query map; the parameter still carries a valid
+    // map (the K map) rather than uninitialised bytes.
     aa.q_tma = (G <= kNarrowRows && (G * d.head_dim * 2) % 1024 == 0) ? 1 : 0;
     if (aa.q_tma) {
       if (!encode_query_map(&mq, q, dims)) return VAS_E_CUDA;
