@@ -389,7 +389,6 @@ struct AttnArgs {
   int32_t T, Hq, Hkv, G, maxp, num_pages, P;
   float scale_log2;  // softmax scale * log2(e)
   float scale;
-  int32_t q_tma;     // the producer brings a decode unit's query rows with TMA
   int32_t* err;
 };
 
@@ -408,11 +407,7 @@ struct Smem {
   static constexpr int kWideBytes = kConsumerWarps * 32 * kWideFloats * 4;
   static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
-  // One buffer per unit-ring slot for the query rows of a unit of <= kNarrowRows rows,
-  // brought by TMA in the same 128-byte-swizzled row layout as the K/V stages.
-  static constexpr int kQBufBytes = kNarrowRows * D * 2;
-  static constexpr int kQRingOff = kSlots * kStageBytes;
-  static constexpr int kScratchOff = kQRingOff + kRing * kQBufBytes;
+  static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
   static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
   // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing] | meta[kSlots], flag[4]
@@ -667,21 +662,6 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
   }
 }
 
-// Whether the producer brings this unit's query rows into its ring buffer by TMA (the
-// same test on both sides): a row block of <= kNarrowRows rows made of whole query
-// tokens.  *j0 / *nj: its first query token and token count.
-__device__ __forceinline__ bool unit_q_in_ring(const AttnArgs& a, const Item& it,
-                                               const SeqPlan& sp, int* j0, int* nj) {
-  if (!a.q_tma || it.seq < 0) return false;
-  const int R = a.G * sp.qlen;
-  const int r0 = (it.split_rb & ((1 << kRbBits) - 1)) * kRowBlock;
-  const int Rb = min(kRowBlock, R - r0);
-  if (Rb > kNarrowRows || r0 % a.G != 0 || Rb % a.G != 0) return false;
-  *j0 = r0 / a.G;
-  *nj = Rb / a.G;
-  return true;
-}
-
 // ---- output helpers ----------------------------------------------------------------
 __device__ __forceinline__ size_t out_row(const AttnArgs& a, const SeqPlan& sp, int head, int r) {
   const int j = r / a.G, hh = r % a.G;
@@ -786,8 +766,7 @@ __device__ __forceinline__ void finish_pending(const AttnArgs& a, PendingMerge& 
 template <int D, int P>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
+                     const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
   using S = Smem<D>;
   constexpr int PPS = kStageTokens / P;  // pages per stage
   constexpr int kPageBytes = P * D * 2;  // one page of one head, one operand
@@ -795,7 +774,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint8_t* qring = smem + S::kQRingOff;
   uint8_t* scratch = smem + S::kScratchOff;
   RingEntry* ring = reinterpret_cast<RingEntry*>(smem + S::kRingOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
@@ -820,7 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps && lane == 0) {
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
-    if (a.q_tma) prefetch_tensor_map(&tm_q);
   }
   __syncthreads();
   pdl_wait_prior_grid();  // the plan of this call is complete and visible
@@ -830,7 +807,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
     const uint64_t pol = l2_policy_evict_first();
-    const uint64_t pol_q = l2_policy_evict_last();  // query rows are read by every split
     uint32_t stage_it = 0, unit_it = 0;
     bool ok = true;
     // Descriptor pipeline: unit u is streamed while the next unit's descriptor and
@@ -875,18 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         e.sp = sp;
         e.pad[0] = e.pad[1] = 0;
         ring[slot] = e;
-        int j0 = 0, nj = 0;
-        if (unit_q_in_ring(a, it, sp, &j0, &nj)) {
-          // A narrow row block: its query rows, token by token, land in this ring slot's
-          // buffer; the consumers' wait on ufull covers them.
-          mbar_arrive_expect_tx(&ufull[slot], (uint32_t)(nj * a.G * D * 2));
-          uint8_t* qdst = qring + slot * S::kQBufBytes;
-          for (int j = 0; j < nj; ++j)
-            tma_load_4d(qdst + j * a.G * D * 2, &tm_q, &ufull[slot], 0, 0, (u % a.Hkv) * a.G,
-                        sp.qrow0 + j0 + j, pol_q);
-        } else {
-          mbar_arrive(&ufull[slot]);
-        }
+        mbar_arrive(&ufull[slot]);
       }
       ++unit_it;
       // Prefetch the next unit's first block-table chunk and the descriptor after it.
@@ -974,6 +939,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     RingEntry re;
     re.u = -1;
     if (got) re = ring[slot];
+    // The slot goes back to the producer at once: holding it to the end of the unit caps
+    // the producer at kRing units ahead of the oldest unit in flight, which measured
+    // slower on long mixed batches.
+    __syncwarp();
+    if (lane == 0 && got) mbar_arrive(&uempty[slot]);
     ++unit_it;
     // Every consumer warp takes the same decision (a warp that left alone would strand
     // the others at a named barrier); this barrier also frees the scratch area of the
@@ -986,10 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (re.u < 0) break;
     const Item it = re.item;
-    if (it.seq < 0) {
-      if (lane == 0) mbar_arrive(&uempty[slot]);
-      continue;
-    }
+    if (it.seq < 0) continue;
     const SeqPlan sp = re.sp;
     const int head = re.head;
     const int split = it.split_rb >> kRbBits, rb = it.split_rb & ((1 << kRbBits) - 1);
@@ -1001,13 +968,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage0 = stage_it;  // first stage of this unit in the CTA's stream
     const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
 
-    // Query rows (row r: token r / G, head head * G + r % G).  A unit the producer
-    // brought them for reads them from its ring buffer; otherwise they are staged here,
-    // rows past Rb up to the MMA tile zero.
-    int qj0, qnj;
-    const bool q_in_ring = unit_q_in_ring(a, it, sp, &qj0, &qnj);
-    const uint8_t* qbuf = qring + slot * S::kQBufBytes;
-    if (!q_in_ring) {
+    // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
+    // past Rb up to the MMA tile are zero.
+    {
       constexpr int kChunks = D / 8;
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
       const int rows_pad = Rb <= 8 ? 8 : ((Rb + 15) & ~15);
@@ -1033,11 +996,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int nn = 0; nn < NN; ++nn) {
             const int row = 8 * nn + (lane & 7);
             const int ch = 4 * kp + (lane >> 3);
-            // Rows past Rb in the ring buffer hold an older unit's rows: they only feed
-            // output columns that are never written.
-            const uint32_t qaddr = q_in_ring ? smem_u32(qbuf) + kv_off<D>(row, ch)
-                                             : smem_u32(scratch + row * S::kQStride + ch * 16);
-            ldsm_x4(qaddr, qb[2 * kp][nn][0], qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0],
+            ldsm_x4(smem_u32(scratch + row * S::kQStride + ch * 16), qb[2 * kp][nn][0],
+                    qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0],
                     qb[2 * kp + 1][nn][1]);
           }
         uint32_t koff[D / 16], voff[D / 16];
@@ -1317,8 +1277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (poison && tid == 0) atomicOr(a.err, VAS_DEV_BAD_PAGE);
     if (sp.nsplit > 1) count_split_arrival(a, sp, it, head, r0, Rb, pm);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&uempty[slot]);  // the unit's ring slot (and query rows) are free
   }
   if (timed_out && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
 }
@@ -1506,26 +1464,9 @@ bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D view of q: (64, D/64, Hq, T) with a (64, D/64, G, 1) box -- the G query heads of
-// one KV head for one query token -- and the 128-byte swizzle.
-bool encode_query_map(CUtensorMap* map, const void* q, const vas_attn_dims* d) {
-  auto fn = get_encode_fn();
-  if (!fn) return false;
-  const int G = d->num_q_heads / d->num_kv_heads;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)d->head_dim / 64, (cuuint64_t)d->num_q_heads,
-                              (cuuint64_t)d->total_q_tokens};
-  const cuuint64_t strides[3] = {128, (cuuint64_t)d->head_dim * 2,
-                                 (cuuint64_t)d->num_q_heads * d->head_dim * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)d->head_dim / 64, (cuuint32_t)G, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, int P>
-int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
-                const AttnArgs& args, int grid, cudaStream_t stream) {
+int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const AttnArgs& args, int grid,
+                cudaStream_t stream) {
   using S = Smem<D>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
@@ -1547,7 +1488,7 @@ int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap&
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, P>, mk, mv, mq, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, P>, mk, mv, args) != cudaSuccess) {
     cudaGetLastError();
     return VAS_E_CUDA;
   }
@@ -1669,29 +1610,17 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   aa.P = d.page_size;
   aa.scale = scale;
   aa.scale_log2 = scale * 1.4426950408889634f;
-  aa.q_tma = 0;
   aa.err = err;
 
   if (bf16) {
-    CUtensorMap mk, mv, mq;
+    CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, k_pages, dims) || !encode_pool_map(&mv, v_pages, dims))
       return VAS_E_CUDA;
-    // The query map brings a decode unit's G rows of one token as one box; it is used
-    // when G <= 16 and each token's rows start on a 1024-byte boundary of the buffer,
-    // where the 128-byte swizzle pattern restarts.
-    // Otherwise the kernel never reads the query map; the parameter still carries a valid
-    // map (the K map) rather than uninitialised bytes.
-    aa.q_tma = (G <= kNarrowRows && (G * d.head_dim * 2) % 1024 == 0) ? 1 : 0;
-    if (aa.q_tma) {
-      if (!encode_query_map(&mq, q, dims)) return VAS_E_CUDA;
-    } else {
-      mq = mk;
-    }
     const int grid = sms;
-    if (d.head_dim == 128 && d.page_size == 16) return launch_bf16<128, 16>(mk, mv, mq, aa, grid, stream);
-    if (d.head_dim == 128) return launch_bf16<128, 32>(mk, mv, mq, aa, grid, stream);
-    if (d.page_size == 16) return launch_bf16<64, 16>(mk, mv, mq, aa, grid, stream);
-    return launch_bf16<64, 32>(mk, mv, mq, aa, grid, stream);
+    if (d.head_dim == 128 && d.page_size == 16) return launch_bf16<128, 16>(mk, mv, aa, grid, stream);
+    if (d.head_dim == 128) return launch_bf16<128, 32>(mk, mv, aa, grid, stream);
+    if (d.page_size == 16) return launch_bf16<64, 16>(mk, mv, aa, grid, stream);
+    return launch_bf16<64, 32>(mk, mv, aa, grid, stream);
   }
   const int grid = 4 * sms;
   if (d.head_dim == 128) attn_f32_kernel<128><<<grid, 128, 0, stream>>>(aa);
