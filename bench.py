@@ -228,11 +228,17 @@ def cpu_baseline(a, v, name):
     import oracle
     w = a
     seqs, smp, dt = choose_oracle_sample(a, 10.0)
+    runs = 1
+    if dt < 10.0:  # the whole batch takes less than the target: run it again
+        extra = int(np.ceil(10.0 / max(dt, 1e-3))) - 1
+        for _ in range(extra):
+            dt += time_oracle_attention(smp, a.kv_dtype)
+        runs += extra
     by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
-                    w.page_size, 2 if w.kv_dtype == "bf16" else 4)
+                    w.page_size, 2 if w.kv_dtype == "bf16" else 4) * runs
     out = {"value": by / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-           "sample": f"paged attention on {len(seqs)} of {a.num_seqs} sequences of {name} "
-                     f"({by / 1e9:.3f} GB algorithmic, {dt:.1f} s)"}
+           "sample": f"paged attention on {len(seqs)} of {a.num_seqs} sequences of {name}, "
+                     f"{runs} run(s) ({by / 1e9:.3f} GB algorithmic, {dt:.1f} s)"}
     if v is not None:
         t0 = time.perf_counter()
         oracle.spec_verify(v.p, v.q, v.draft, v.seed)
