@@ -15,7 +15,8 @@
 //                       dependent of the plan.  A producer warp takes work units (work
 //                       item x KV head) from an atomic counter and streams the unit's
 //                       K/V page slices into an 8-slot ring of 32-token stages with TMA
-//                       (one 4-D box per page and operand, 128-byte swizzle), tracked by
+//                       (each 64-column half of a stage operand a tile of its own,
+//                       128-byte swizzle), tracked by
 //                       mbarriers; it prefetches the next unit's descriptor and block-
 //                       table entries while streaming.  Four consumer warps compute on
 //                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32):
@@ -416,14 +417,15 @@ struct Smem {
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-// Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage:
-// the TMA box lands as [token][D/64 halves][64] with the 128-byte swizzle, i.e. the
-// chunk index is XOR-ed with the index of its 128-byte row modulo 8.
+// Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage.
+// Each 64-column half of the operand is its own tile of kStageTokens rows of 128 bytes
+// ([D/64 halves][token][64], one TMA box per page and half), with the 128-byte swizzle:
+// the chunk index is XOR-ed with the token row modulo 8.  A half tile is the canonical
+// K-major (for K) and MN-major (for V) 128-byte-swizzled operand layout of tcgen05.
+constexpr int kHalfBytes = kStageTokens * 128;
 template <int D>
 __device__ __forceinline__ uint32_t kv_off(int t, int gc) {
-  constexpr int NH = D / 64;
-  const int row = t * NH + (gc >> 3);
-  return (uint32_t)(row * 128 + (((gc & 7) ^ (row & 7)) << 4));
+  return (uint32_t)((gc >> 3) * kHalfBytes + t * 128 + (((gc & 7) ^ (t & 7)) << 4));
 }
 
 // Conditional rescaling.  Probabilities are taken against a per-row reference maximum
@@ -455,7 +457,7 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
                                              float (&oT)[D / 16][NN][4], float (&mref)[NN][2],
                                              float (&l)[NN][2], int t_abs0,
                                              const int (&lim)[NN][2], float c, int lane) {
-  constexpr uint32_t kTile = 16 * D * 2;  // bytes of 16 token rows
+  constexpr uint32_t kTile = 16 * 128;  // 16 token rows of a half tile
   const int g = lane >> 2;
   float s[2][NN][4];
 #pragma unroll
@@ -594,7 +596,7 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
 #pragma unroll
       for (int qd = 0; qd < D / 32; ++qd) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + kw[qd] + nt * (8 * D * 2), b0, b1, b2, b3);
+        ldsm_x4(kbase + kw[qd] + nt * (8 * 128), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
         mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
       }
@@ -654,7 +656,7 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vbase + vw[dp] + kk * (16 * D * 2), b0, b1, b2, b3);
+        ldsm_x4_trans(vbase + vw[dp] + kk * (16 * 128), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dp], pa, b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
@@ -895,8 +897,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < PPS; ++e) {
                 if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
-                  tma_load_4d(kdst + e * kPageBytes, &tm_k, &full[slot_s], 0, 0, head, ids[e] * P, pol);
-                  tma_load_4d(vdst + e * kPageBytes, &tm_v, &full[slot_s], 0, 0, head, ids[e] * P, pol);
+                  if (PPS == 1) {  // one box: both halves of the page
+                    tma_load_4d(kdst, &tm_k, &full[slot_s], 0, ids[e] * P, 0, head, pol);
+                    tma_load_4d(vdst, &tm_v, &full[slot_s], 0, ids[e] * P, 0, head, pol);
+                  } else {
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                      const int off = h * kHalfBytes + e * P * 128;
+                      tma_load_4d(kdst + off, &tm_k, &full[slot_s], 0, ids[e] * P, h, head, pol);
+                      tma_load_4d(vdst + off, &tm_v, &full[slot_s], 0, ids[e] * P, h, head, pol);
+                    }
+                  }
                 }
               }
             }
@@ -1182,7 +1193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
             }
             const bool interior = tvalid == TS && t_abs0 + ts0 + TS - 1 <= min_lim;
-            const uint32_t ks = kbase + ts0 * (D * 2), vs = vbase + ts0 * (D * 2);
+            const uint32_t ks = kbase + ts0 * 128, vs = vbase + ts0 * 128;
             const int ta = t_abs0 + ts0;
             if (TS == 16) {
               if (interior)
@@ -1448,16 +1459,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 4-D view of a page pool: (64, D/64, Hkv, num_pages * P) with a (64, D/64, 1, P) box --
-// one page of one KV head -- and the 128-byte swizzle.
+// 4-D view of a page pool with the token before the column half:
+// (64, num_pages * P, D/64, Hkv), strides (Hkv*D*2, 128, D*2) bytes, 128-byte swizzle.
+// A box of (64, P, halves, 1) then lands as [half][token][64]: with 32-token pages one box
+// fills a whole stage operand ([D/64][32 tokens]); with 16-token pages each half of a page
+// is its own box.
 bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d) {
   auto fn = get_encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[4] = {64, (cuuint64_t)d->head_dim / 64, (cuuint64_t)d->num_kv_heads,
-                              (cuuint64_t)d->num_pages * d->page_size};
-  const cuuint64_t strides[3] = {128, (cuuint64_t)d->head_dim * 2,
-                                 (cuuint64_t)d->num_kv_heads * d->head_dim * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)d->head_dim / 64, 1, (cuuint32_t)d->page_size};
+  const cuuint64_t dims[4] = {64, (cuuint64_t)d->num_pages * d->page_size,
+                              (cuuint64_t)d->head_dim / 64, (cuuint64_t)d->num_kv_heads};
+  const cuuint64_t strides[3] = {(cuuint64_t)d->num_kv_heads * d->head_dim * 2, 128,
+                                 (cuuint64_t)d->head_dim * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size,
+                             d->page_size == 32 ? (cuuint32_t)d->head_dim / 64 : 1u, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
