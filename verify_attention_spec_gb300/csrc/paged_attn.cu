@@ -57,7 +57,11 @@ constexpr int kStageTokens = 32;   // KV tokens per pipeline stage
 constexpr int kSlots = 8;          // stages in the shared-memory ring
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kProducerWarp = kConsumerWarps;      // TMA loads
+constexpr int kMmaWarp = kConsumerWarps + 1;       // tcgen05 issue for wide units
+constexpr int kThreads = kConsumerThreads + 64;    // + producer warp + MMA warp
+constexpr int kTmemCols = 128;                     // O of a wide unit: 128 lanes x D fp32
+constexpr int kTmemO = 0;
 constexpr int kRowBlock = 64;      // query rows per unit (four m16 tiles)
 // In a decode unit warp w consumes the stages s with s % kConsumerWarps == w and waits
 // on slot s % kSlots by phase parity.  The parity test is only sound if the slot's
@@ -404,15 +408,22 @@ struct Smem {
   static constexpr int kNarrowStride = D + 4;               // floats per merge row
   static constexpr int kNarrowWarpFloats = kNarrowRows * kNarrowStride + 2 * kNarrowRows;
   static constexpr int kNarrowBytes = kConsumerWarps * kNarrowWarpFloats * 4;
-  static constexpr int kWideFloats = (D / 8) * 4 + 4;       // per thread: O frags + m,l x2
-  static constexpr int kWideBytes = kConsumerWarps * 32 * kWideFloats * 4;
+  // Wide units: two P tiles of the tcgen05 PV product (by step parity), each 128 rows
+  // (TMEM lanes) of 128 bytes -- the 64 tokens of a two-stage step -- in the K-major
+  // 128-byte-swizzled layout.  They reuse the query staging, which is dead once the
+  // warps hold their query fragments.
+  static constexpr int kPTileOff = 0;
+  static constexpr int kPTileBytes = 128 * 128;
+  static constexpr int kWideBytes = kPTileOff + 2 * kPTileBytes;
   static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
   static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
-  // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing] | meta[kSlots], flag[4]
-  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing) * 8 + (kSlots + 4) * 4;
+  // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing], wide unit barriers
+  // bp[2], bo[2], bfin | meta[kSlots], flag[4], tmem base
+  static constexpr int kWideBars = 5;
+  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars) * 8 + (kSlots + 4 + 1) * 4;
   static constexpr int kBytes = kBarOff + kBarBytes;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -564,51 +575,53 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
   }
 }
 
-// Per-lane ldmatrix byte offsets for the wide path: kw[qd]: K B-fragments of token
-// tile 0 (8 rows), d-chunks 4qd..4qd+3; vw[dp]: V B-fragments of token tile 0 (16
-// rows), d-tiles 2dp, 2dp+1.
+// Per-lane ldmatrix byte offsets of the K B-fragments of the wide path: token tile 0
+// (8 rows), d-chunks 4 qd .. 4 qd + 3.
 template <int D>
-__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32],
-                                             uint32_t (&vw)[D / 16]) {
+__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32]) {
   const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D>(r8, 4 * i + mi);
-#pragma unroll
-  for (int i = 0; i < D / 16; ++i) vw[i] = kv_off<D>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
 }
 
-// ---- wide units: S = Q K^T, warps split m16 row tiles and token slices --------------
-// kbase / vbase point at this warp's token slice.
-template <int D, int TS, bool MASKED>
-__device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int tvalid,
-                                           const uint32_t (&qa)[D / 16][4],
-                                           const uint32_t (&kw)[D / 32],
-                                           const uint32_t (&vw)[D / 16], float (&o)[D / 8][4],
-                                           float (&mref)[2], float (&l)[2], int t_abs_slice,
-                                           int limA, int limB, float c, int lane) {
-  constexpr int NT = TS / 8;
-  const int tq = lane & 3;
+// ---- wide units: S = Q K^T of one m16 row tile over a step, in registers -------------
+// A step is NST (1 or 2) consecutive 32-token stages of the unit: token tt of the step
+// lies in stage tt / 32 (K tile kb[tt / 32]).  Warp MMA for the scores (rows g and g + 8
+// of the tile, tokens 8 nt + 2 tq + {0, 1}), online softmax with the conditional
+// rescaling, and P as bf16 into this warp's 16 rows of the step's P tile (prow: the tile
+// row of row g; byte 2 tt of a row before the swizzle).  alpha / rescale report a moved
+// reference maximum: O, held in TMEM, is rescaled by the caller.
+template <int D, int NST>
+__device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid, bool masked,
+                                            const uint32_t (&qa)[D / 16][4],
+                                            const uint32_t (&kw)[D / 32], float (&mref)[2],
+                                            float (&l)[2], float (&alpha)[2], bool& rescale,
+                                            int t_abs0, int limA, int limB, float c, int lane,
+                                            uint8_t* prow) {
+  constexpr int NT = 4 * NST;
+  const int g = lane >> 2, tq = lane & 3;
   float s[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    if (!MASKED || 8 * nt < tvalid) {
+  for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+  // k-steps outside, token tiles inside: independent accumulation chains in flight.
+  // Every tile is computed (rows of a stage past its loaded tokens are stale but inside
+  // the tile, and masked below), so the products carry no branches.
 #pragma unroll
-      for (int qd = 0; qd < D / 32; ++qd) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + kw[qd] + nt * (8 * 128), b0, b1, b2, b3);
-        mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
-        mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
-      }
+  for (int qd = 0; qd < D / 32; ++qd)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb[nt >> 2] + kw[qd] + (nt & 3) * (8 * 128), b0, b1, b2, b3);
+      mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
+      mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
     }
-  }
-  if (MASKED) {
+  if (masked) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tt = 8 * nt + 2 * tq + (e & 1);
-        if (tt >= tvalid || t_abs_slice + tt > ((e < 2) ? limA : limB)) s[nt][e] = -INFINITY;
+        if (tt >= tvalid || t_abs0 + tt > ((e < 2) ? limA : limB)) s[nt][e] = -INFINITY;
       }
   }
   float mx[2] = {-INFINITY, -INFINITY};
@@ -616,6 +629,8 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
+  alpha[0] = alpha[1] = 1.f;
+  rescale = false;
   const bool up = mx[0] * c > mref[0] + kRebase || mx[1] * c > mref[1] + kRebase;
   if (__any_sync(0xffffffffu, up)) {
 #pragma unroll
@@ -625,42 +640,26 @@ __device__ __forceinline__ void wide_stage(uint32_t kbase, uint32_t vbase, int t
       v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
       const float vs = v * c;
       if (vs > mref[h] + kRebase) {  // same decision on the quad sharing the row
-        const float alpha = exp2f(mref[h] - vs);
-        l[h] *= alpha;
-#pragma unroll
-        for (int dt = 0; dt < D / 8; ++dt) {
-          o[dt][2 * h] *= alpha;
-          o[dt][2 * h + 1] *= alpha;
-        }
+        if (mref[h] != -INFINITY) rescale = true;
+        alpha[h] = exp2f(mref[h] - vs);
+        l[h] *= alpha[h];
         mref[h] = vs;
       }
     }
   }
   const float nm[2] = {mref[0] == -INFINITY ? 0.f : -mref[0], mref[1] == -INFINITY ? 0.f : -mref[1]};
+  // Rows g and g + 8 share the swizzle (tile rows 32 w + g, 32 w + g + 8).
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int nt = 0; nt < NT; ++nt) {
+    float p[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float p = exp2f(fmaf(s[nt][e], c, nm[e >> 1]));
-      s[nt][e] = p;
-      l[e >> 1] += p;
+      p[e] = ex2_approx(fmaf(s[nt][e], c, nm[e >> 1]));
+      l[e >> 1] += p[e];
     }
-#pragma unroll
-  for (int kk = 0; kk < TS / 16; ++kk) {
-    if (!MASKED || 16 * kk < tvalid) {
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vbase + vw[dp] + kk * (16 * 128), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dp], pa, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
-      }
-    }
+    const int off = ((nt ^ g) << 4) + 4 * tq;
+    *reinterpret_cast<uint32_t*>(prow + off) = pack_bf16x2(p[0], p[1]);
+    *reinterpret_cast<uint32_t*>(prow + 8 * 128 + off) = pack_bf16x2(p[2], p[3]);
   }
 }
 
@@ -782,31 +781,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kSlots;
   uint64_t* ufull = empty + kSlots;
   uint64_t* uempty = ufull + kRing;
-  int32_t* meta = reinterpret_cast<int32_t*>(uempty + kRing);
+  // Wide units: bp[b] P of the stage with parity b is in shared memory; bo[b] the PV
+  // product of that stage is done; bfin every tcgen05.mma of the CTA has completed.
+  uint64_t* bp = uempty + kRing;
+  uint64_t* bo = bp + 2;
+  uint64_t* bfin = bo + 2;
+  int32_t* meta = reinterpret_cast<int32_t*>(bfin + 1);
   int32_t* flag = meta + kSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flag + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], 1);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&ufull[r], 1);
-      mbar_init(&uempty[r], kConsumerWarps);
+      mbar_init(&uempty[r], kConsumerWarps + 1);  // consumers and the MMA warp
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bp[b], kConsumerWarps);
+      mbar_init(&bo[b], 1);
+    }
+    mbar_init(bfin, 1);
     mbar_fence_init();
   }
-  if (warp == kConsumerWarps && lane == 0) {
+  if (warp == kProducerWarp && lane == 0) {
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
   }
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);  // one CTA per SM: never contended
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_wait_prior_grid();  // the plan of this call is complete and visible
 
   const int32_t n_units = a.header->n_items * a.Hkv;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------ producer ------------------------------
     const uint64_t pol = l2_policy_evict_first();
     uint32_t stage_it = 0, unit_it = 0;
@@ -934,11 +948,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
+  if (warp == kMmaWarp) {
+    // ------------------------------ MMA warp ------------------------------
+    // Follows the unit ring like the consumers.  A wide unit is taken in steps of two
+    // 32-token stages (one at an odd end).  For step k (parity b = k & 1), once the
+    // consumer warps have written P tile b (bp[b]), it issues O += P_b V in TMEM (M 128
+    // lanes, N = D, 16 tokens per product over the step's loaded tokens) and commits
+    // to the stages' empty barriers (they may be refilled) and to bo[b].  Lane 0
+    // issues; the warp waits together.
+    uint32_t stage_it = 0, unit_it = 0, wk = 0;
+    bool ok = true;
+    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, false, true);
+    // All operands are 128-byte swizzled with 1024-byte 8-row groups: the high descriptor
+    // word is shared, the low word carries the start address.
+    constexpr uint32_t kDescHi = umma_desc_hi_sw128(1024);
+    const uint32_t p_lo = umma_desc_lo(smem_u32(scratch + S::kPTileOff), 16);  // P tile 0
+    for (;;) {
+      const int slot = unit_it % kRing;
+      if (!mbar_wait(&ufull[slot], (unit_it / kRing) & 1)) {
+        ok = false;
+        break;
+      }
+      const RingEntry re = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&uempty[slot]);
+      ++unit_it;
+      if (re.u < 0) break;
+      const Item it = re.item;
+      if (it.seq < 0) continue;
+      const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
+      const int R = a.G * re.sp.qlen;
+      const int Rb = min(kRowBlock, R - (it.split_rb & ((1 << kRbBits) - 1)) * kRowBlock);
+      if (Rb <= kNarrowRows || n_stages == 0) {  // consumed by the consumer warps alone
+        stage_it += n_stages;
+        continue;
+      }
+      const int n_steps = (n_stages + 1) >> 1;
+      for (int j = 0; j < n_steps; ++j) {
+        const uint32_t k = wk + j, b = k & 1;
+        if (!mbar_wait(&bp[b], (k >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
+          for (int h = 0; h < 2 && 2 * j + h < n_stages; ++h) {
+            const uint32_t st = stage_it + 2 * j + h;
+            const int slot_s = st % kSlots;
+            const int pg = it.page_begin + (2 * j + h) * PPS;
+            const int loaded = min(PPS, it.page_end - pg) * P;
+            const uint32_t v_lo = umma_desc_lo(
+                smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), kHalfBytes);
+            for (int kk = 0; kk < loaded / 16; ++kk)
+              umma_bf16_lh(tmem + kTmemO, pb_lo + ((h * 64 + kk * 32) >> 4),
+                           v_lo + ((kk * 16 * 128) >> 4), kDescHi, kIdO, j > 0 || h > 0 || kk > 0);
+            umma_commit(&empty[slot_s]);
+          }
+          umma_commit(&bo[b]);
+        }
+        __syncwarp();
+      }
+      wk += n_steps;
+      stage_it += n_stages;
+      if (!ok) break;
+    }
+    // Tensor memory is freed only after every product this warp issued has completed.
+    if (lane == 0) umma_commit(bfin);
+    __syncwarp();
+    if (!mbar_wait(bfin, 0)) ok = false;
+    if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
+    tc_fence_before();
+    named_bar_sync(2, kConsumerThreads + 32);
+    return;
+  }
+
   // -------------------------------- consumers --------------------------------
   const int tid = threadIdx.x;  // 0 .. kConsumerThreads-1
   const int g = lane >> 2, tq = lane & 3;
   const float kLn2 = 0.6931471805599453f;
   uint32_t stage_it = 0, unit_it = 0;
+  uint32_t wk = 0;  // stages of wide units so far (the MMA warp counts the same)
   bool timed_out = false;
   PendingMerge pm;
   pm.valid = 0;
@@ -979,9 +1069,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t stage0 = stage_it;  // first stage of this unit in the CTA's stream
     const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
 
-    // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
-    // past Rb up to the MMA tile are zero.
+    const bool wide = Rb > kNarrowRows && n_stages > 0;
     {
+      // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
+      // past Rb up to the MMA tile are zero.
       constexpr int kChunks = D / 8;
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
       const int rows_pad = Rb <= 8 ? 8 : ((Rb + 15) & ~15);
@@ -996,7 +1087,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     bool poison = false;
-    if (Rb <= kNarrowRows) {
+    if (!wide) {
       // ============================ narrow unit ============================
       auto run = [&](auto nn_tag) {
         constexpr int NN = decltype(nn_tag)::value;
@@ -1061,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             narrow_stage<D, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
                                       lim, a.scale_log2, lane);
           __syncwarp();
-          if (lane == 0) mbar_arrive_count(&empty[slot_s], kConsumerWarps);
+          if (lane == 0) mbar_arrive(&empty[slot_s]);
         }
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn)
@@ -1138,16 +1229,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ============================= wide unit =============================
+      // Warp w < nM owns m16 row tile w (rows 16 w .. 16 w + 15): S = Q K^T by warp MMA
+      // and the softmax in registers, P into tile rows 32 w + (0 .. 15) (TMEM lanes of
+      // this warp).  The MMA warp accumulates O = P V in TMEM with tcgen05; thread t < 16
+      // of warp w reads, rescales and finally writes O row 16 w + t.
       const int nM = (Rb + 15) >> 4;
-      const int nW = nM == 2 ? 2 : 1;
-      const bool active = warp < nM * nW;
-      const int mt = warp % nM;
-      const int slice = warp / nM;
-      const int TS = kStageTokens / nW;
+      const bool active = warp < nM;
+      const int g = lane >> 2;
       uint32_t qa[D / 16][4];
       if (active) {
         const int mi = lane >> 3;
-        const int row = 16 * mt + (mi & 1) * 8 + (lane & 7);
+        const int row = 16 * warp + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int ch = 2 * ks + (mi >> 1);
@@ -1155,141 +1247,167 @@ __global__ void __launch_bounds__(kThreads, 1)
                   qa[ks][2], qa[ks][3]);
         }
       }
-      uint32_t kw[D / 32], vw[D / 16];
-      wide_offsets<D>(lane, kw, vw);
-      float o[D / 8][4];
-#pragma unroll
-      for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-      float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-      const int rA = r0 + 16 * mt + g, rB = rA + 8;
+      uint32_t kw[D / 32];
+      wide_offsets<D>(lane, kw);
+      named_bar_sync(1, kConsumerThreads);  // the query staging becomes the P tiles
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      float mref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+      const int rA = r0 + 16 * warp + g, rB = rA + 8;
       const int limA = rA < R ? L - ql + rA / a.G : L - 1;
       const int limB = rB < R ? L - ql + rB / a.G : L - 1;
-      for (int si = 0; si < n_stages; ++si, ++stage_it) {
-        const int slot_s = stage_it % kSlots;
-        if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+      const int n_steps = (n_stages + 1) >> 1;
+      for (int sj = 0; sj < n_steps; ++sj) {
+        const uint32_t k = wk + sj, b = k & 1;
+        const int nst = min(2, n_stages - 2 * sj);
+        // Both stages of the step are loaded (and their V rows past the sequence end
+        // zeroed: those slots may hold anything, NaN included, and meet P = 0).
+        uint32_t kb[2];
+        int loaded = 0;
+        bool got = true;
+        const int t_abs0 = (it.page_begin + 2 * sj * PPS) * P;
+        for (int h = 0; h < nst; ++h) {
+          const uint32_t st = stage_it + h;
+          const int slot_s = st % kSlots;
+          got = got && mbar_wait_fast(&full[slot_s], (st / kSlots) & 1);
+          if (meta[slot_s]) poison = true;
+          const int pg = it.page_begin + (2 * sj + h) * PPS;
+          const int ld = min(PPS, it.page_end - pg) * P;
+          kb[h] = smem_u32(stages + slot_s * S::kStageBytes);
+          const int ta = pg * P;
+          if (ta + ld > L) {
+            uint8_t* vt = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+            const int z0 = max(0, L - ta);
+            for (int cc = z0 * (D / 8) + tid; cc < ld * (D / 8); cc += kConsumerThreads)
+              *reinterpret_cast<uint4*>(vt + kv_off<D>(cc / (D / 8), cc % (D / 8))) =
+                  make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+          }
+          loaded += ld;
+        }
+        if (nst == 1) kb[1] = kb[0];
+        if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
           timed_out = true;
-          stage_it += n_stages - si;
+          stage_it += n_stages - 2 * sj;
           break;
         }
-        if (meta[slot_s]) poison = true;
-        const int pg = it.page_begin + si * PPS;
-        const int loaded = min(PPS, it.page_end - pg) * P;
-        const int t_abs0 = pg * P;
-        const uint32_t kbase = smem_u32(stages + slot_s * S::kStageBytes);
-        const uint32_t vbase = kbase + S::kOperandBytes;
+        stage_it += nst;
+        // P tile b was last read by the product two steps back.  Every warp waits for
+        // it, idle ones included: a warp that arrived on bp[b] for step k before that
+        // product was issued would be counted in the phase of step k - 2.
+        if (k >= 2 && !mbar_wait_fast(&bo[b], ((k - 2) >> 1) & 1)) timed_out = true;
         if (active) {
-          const int ts0 = slice * TS;
-          const int tvalid = min(TS, loaded - ts0);
-          if (tvalid > 0) {
-            if (t_abs0 + ts0 + tvalid > L) {
-              // Several warps read these rows: each zeroes them before its own reads
-              // (all write the same zeros).
-              uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
-              const int z0 = max(0, L - t_abs0 - ts0);
-              for (int c = z0 * (D / 8) + lane; c < tvalid * (D / 8); c += 32)
-                *reinterpret_cast<uint4*>(vrow + kv_off<D>(ts0 + c / (D / 8), c % (D / 8))) =
-                    make_uint4(0, 0, 0, 0);
-              fence_proxy_async_smem();
-              __syncwarp();
-            }
-            const bool interior = tvalid == TS && t_abs0 + ts0 + TS - 1 <= min_lim;
-            const uint32_t ks = kbase + ts0 * 128, vs = vbase + ts0 * 128;
-            const int ta = t_abs0 + ts0;
-            if (TS == 16) {
-              if (interior)
-                wide_stage<D, 16, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
-              else
-                wide_stage<D, 16, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
-            } else {
-              if (interior)
-                wide_stage<D, 32, false>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
-              else
-                wide_stage<D, 32, true>(ks, vs, tvalid, qa, kw, vw, o, m, l, ta, limA, limB, a.scale_log2, lane);
+          tc_fence_after();
+          uint8_t* prow = scratch + S::kPTileOff + b * S::kPTileBytes + (32 * warp + g) * 128;
+          // Masking is a runtime switch: a separate unmasked instantiation would cost the
+          // whole kernel register spills.
+          const bool masked = loaded < 2 * kStageTokens || t_abs0 + 2 * kStageTokens - 1 > min_lim;
+          float alpha[2];
+          bool rescale;
+          if (nst == 2)
+            wide_s_step<D, 2>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
+                              limB, a.scale_log2, lane, prow);
+          else
+            wide_s_step<D, 1>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
+                              limB, a.scale_log2, lane, prow);
+          if (__any_sync(0xffffffffu, rescale && sj > 0)) {
+            // O holds the products up to the previous step: wait for the last of them,
+            // then scale row 16 w + t (lane t < 16) by its factor (held by lane 4 (t % 8)).
+            const uint32_t kp = k - 1;
+            if (!mbar_wait(&bo[kp & 1], (kp >> 1) & 1)) timed_out = true;
+            tc_fence_after();
+            const float f0 = __shfl_sync(0xffffffffu, alpha[0], 4 * (lane & 7));
+            const float f1 = __shfl_sync(0xffffffffu, alpha[1], 4 * (lane & 7));
+            const float f = lane < 8 ? f0 : (lane < 16 ? f1 : 1.f);
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t ov[32];
+              tmem_ld32(tmem + lane_base + kTmemO + cc * 32, ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+              tmem_st32(tmem + lane_base + kTmemO + cc * 32, ov);
             }
           }
+          fence_proxy_async_smem();
         }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot_s]);
+        if (lane == 0) mbar_arrive(&bp[b]);
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+      // The unit's last product (it covers every earlier one).
+      if (!timed_out) {
+        const uint32_t kl = wk + n_steps - 1;
+        if (!mbar_wait(&bo[kl & 1], (kl >> 1) & 1)) timed_out = true;
       }
-      float* cb = reinterpret_cast<float*>(scratch);
-      named_bar_sync(1, kConsumerThreads);  // everyone is done with the Q rows
-      if (active && nW > 1 && slice > 0) {
-        float* mine = cb + (size_t)warp * 32 * S::kWideFloats;
-#pragma unroll
-        for (int dt = 0; dt < D / 8; ++dt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) mine[(dt * 4 + e) * 32 + lane] = o[dt][e];
-        mine[(D / 2 + 0) * 32 + lane] = m[0];
-        mine[(D / 2 + 1) * 32 + lane] = m[1];
-        mine[(D / 2 + 2) * 32 + lane] = l[0];
-        mine[(D / 2 + 3) * 32 + lane] = l[1];
-      }
+      wk += n_steps;
+      tc_fence_after();
       poison = named_bar_or(1, kConsumerThreads, poison);
       if (named_bar_or(1, kConsumerThreads, timed_out)) {
         timed_out = true;
         break;
       }
-      if (active && slice == 0) {
-        for (int sl = 1; sl < nW; ++sl) {
-          const float* other = cb + (size_t)(mt + sl * nM) * 32 * S::kWideFloats;
-          const float om[2] = {other[(D / 2 + 0) * 32 + lane], other[(D / 2 + 1) * 32 + lane]};
-          const float ol[2] = {other[(D / 2 + 2) * 32 + lane], other[(D / 2 + 3) * 32 + lane]};
-          float fa[2], fb[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float mm = fmaxf(m[h], om[h]);
-            const float mu = mm == -INFINITY ? 0.f : mm;
-            fa[h] = exp2f(m[h] - mu);
-            fb[h] = exp2f(om[h] - mu);
-            l[h] = l[h] * fa[h] + ol[h] * fb[h];
-            m[h] = mm;
-          }
-#pragma unroll
-          for (int dt = 0; dt < D / 8; ++dt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              o[dt][e] = o[dt][e] * fa[e >> 1] + other[(dt * 4 + e) * 32 + lane] * fb[e >> 1];
-        }
+      if (active) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int r = h ? rB : rA;
-          if (r >= r0 + Rb) continue;
-          const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
-          float row_lse = l[h] > 0.f ? (m[h] + log2f(l[h])) * kLn2 : -INFINITY;
-          if (poison) row_lse = NAN;
-          if (sp.nsplit == 1) {
-            const size_t orow = out_row(a, sp, head, r);
-            __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.out) + orow * D;
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+          l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+        }
+        // Lane t < 16 writes row 16 w + t: its (m, l) from lane 4 (t % 8), half t / 8.
+        const float mA = __shfl_sync(0xffffffffu, mref[0], 4 * (lane & 7));
+        const float mB = __shfl_sync(0xffffffffu, mref[1], 4 * (lane & 7));
+        const float lA = __shfl_sync(0xffffffffu, l[0], 4 * (lane & 7));
+        const float lB = __shfl_sync(0xffffffffu, l[1], 4 * (lane & 7));
+        const float mm = lane < 8 ? mA : mB, ll = lane < 8 ? lA : lB;
+        const int rr = 16 * warp + lane;
+        const bool row_ok = lane < 16 && rr < Rb;
+        const float inv = ll > 0.f ? 1.f / ll : 0.f;
+        float row_lse = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
+        if (poison) row_lse = NAN;
+        const bool whole = sp.nsplit == 1;
+        const size_t orow = row_ok ? (whole ? out_row(a, sp, head, r0 + rr)
+                                            : partial_row(a, sp, split, head, r0 + rr))
+                                   : 0;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, ov);
+          if (!row_ok) continue;
+          float x[32];
 #pragma unroll
-            for (int dt = 0; dt < D / 8; ++dt) {
-              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
-              if (poison) x0 = x1 = NAN;
-              *reinterpret_cast<uint32_t*>(og + dt * 8 + 2 * tq) = pack_bf16x2(x0, x1);
-            }
-            if (tq == 0) a.lse[orow] = row_lse;
+          for (int i = 0; i < 32; ++i) x[i] = poison ? NAN : __uint_as_float(ov[i]) * inv;
+          if (whole) {
+            uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
+                                                 cc * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              og[q4] = make_uint4(pack_bf16x2(x[8 * q4], x[8 * q4 + 1]),
+                                  pack_bf16x2(x[8 * q4 + 2], x[8 * q4 + 3]),
+                                  pack_bf16x2(x[8 * q4 + 4], x[8 * q4 + 5]),
+                                  pack_bf16x2(x[8 * q4 + 6], x[8 * q4 + 7]));
           } else {
-            const size_t prow = partial_row(a, sp, split, head, r);
-            float* po = a.part_o + prow * D;
+            float4* po = reinterpret_cast<float4*>(a.part_o + orow * D + cc * 32);
 #pragma unroll
-            for (int dt = 0; dt < D / 8; ++dt) {
-              float x0 = o[dt][2 * h] * inv, x1 = o[dt][2 * h + 1] * inv;
-              if (poison) x0 = x1 = NAN;
-              *reinterpret_cast<float2*>(po + dt * 8 + 2 * tq) = make_float2(x0, x1);
-            }
-            if (tq == 0) a.part_lse[prow] = row_lse;
+            for (int q4 = 0; q4 < 8; ++q4)
+              po[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
           }
         }
+        if (row_ok) {
+          if (whole) a.lse[orow] = row_lse;
+          else a.part_lse[orow] = row_lse;
+        }
       }
+      tc_fence_before();
     }
     if (poison && tid == 0) atomicOr(a.err, VAS_DEV_BAD_PAGE);
     if (sp.nsplit > 1) count_split_arrival(a, sp, it, head, r0, Rb, pm);
   }
   if (timed_out && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
+  // Tensor memory goes back once the MMA warp has seen its last product complete.
+  tc_fence_before();
+  named_bar_sync(2, kConsumerThreads + 32);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ------------------------------------------------------------------------------------
