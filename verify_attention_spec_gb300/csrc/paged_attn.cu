@@ -15,8 +15,8 @@
 //                       dependent of the plan.  A producer warp takes work units (work
 //                       item x KV head) from an atomic counter and streams the unit's
 //                       K/V page slices into an 8-slot ring of 32-token stages with TMA
-//                       (each 64-column half of a stage operand a tile of its own,
-//                       128-byte swizzle), tracked by
+//                       (one box per page and operand, landing as [half][token][64]
+//                       with the 128-byte swizzle), tracked by
 //                       mbarriers; it prefetches the next unit's descriptor and block-
 //                       table entries while streaming.  Four consumer warps compute on
 //                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32):
@@ -429,14 +429,20 @@ struct Smem {
 };
 
 // Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage.
-// Each 64-column half of the operand is its own tile of kStageTokens rows of 128 bytes
-// ([D/64 halves][token][64], one TMA box per page and half), with the 128-byte swizzle:
-// the chunk index is XOR-ed with the token row modulo 8.  A half tile is the canonical
-// K-major (for K) and MN-major (for V) 128-byte-swizzled operand layout of tcgen05.
-constexpr int kHalfBytes = kStageTokens * 128;
-template <int D>
+// A stage operand is its pages in order, each page one TMA box laid out as
+// [D/64 halves][P tokens][64] with the 128-byte swizzle (the chunk index XOR-ed with the
+// token row modulo 8).  A page half is the canonical K-major (for K) and MN-major (for V)
+// 128-byte-swizzled operand layout of tcgen05.
+template <int D, int P>
 __device__ __forceinline__ uint32_t kv_off(int t, int gc) {
-  return (uint32_t)((gc >> 3) * kHalfBytes + t * 128 + (((gc & 7) ^ (t & 7)) << 4));
+  return (uint32_t)((t / P) * (P * D * 2) + (gc >> 3) * (P * 128) + (t % P) * 128 +
+                    (((gc & 7) ^ (t & 7)) << 4));
+}
+// Byte offset of token row t (a multiple of 8) in every column half: added to an offset
+// from kv_off for row t0 % 8, it gives row t0 + t.
+template <int D, int P>
+__host__ __device__ constexpr uint32_t tok_off(int t) {
+  return (uint32_t)((t / P) * (P * D * 2) + (t % P) * 128);
 }
 
 // Conditional rescaling.  Probabilities are taken against a per-row reference maximum
@@ -448,19 +454,19 @@ constexpr float kRebase = 8.f;
 // Per-lane ldmatrix byte offsets (relative to a stage operand) for the narrow path:
 // koff[ks]: K A-fragment of token tile 0, k-step ks; voff[dt]: V^T A-fragment of token
 // tile 0, d-tile dt.  Token tile 1 adds 16 rows.
-template <int D>
+template <int D, int P>
 __device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[D / 16],
                                                uint32_t (&voff)[D / 16]) {
   const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
   for (int i = 0; i < D / 16; ++i) {
-    koff[i] = kv_off<D>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
-    voff[i] = kv_off<D>((mi >> 1) * 8 + r8, 2 * i + (mi & 1));
+    koff[i] = kv_off<D, P>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
+    voff[i] = kv_off<D, P>((mi >> 1) * 8 + r8, 2 * i + (mi & 1));
   }
 }
 
 // ---- narrow units: S^T = K Q^T, one warp per stage -------------------------------
-template <int D, int NN, bool MASKED>
+template <int D, int P, int NN, bool MASKED>
 __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int loaded,
                                              const uint32_t (&qb)[D / 16][NN][2],
                                              const uint32_t (&koff)[D / 16],
@@ -468,7 +474,7 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
                                              float (&oT)[D / 16][NN][4], float (&mref)[NN][2],
                                              float (&l)[NN][2], int t_abs0,
                                              const int (&lim)[NN][2], float c, int lane) {
-  constexpr uint32_t kTile = 16 * 128;  // 16 token rows of a half tile
+  constexpr uint32_t kTile = tok_off<D, P>(16);  // 16 token rows
   const int g = lane >> 2;
   float s[2][NN][4];
 #pragma unroll
@@ -577,11 +583,11 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
 
 // Per-lane ldmatrix byte offsets of the K B-fragments of the wide path: token tile 0
 // (8 rows), d-chunks 4 qd .. 4 qd + 3.
-template <int D>
+template <int D, int P>
 __device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32]) {
   const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D>(r8, 4 * i + mi);
+  for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D, P>(r8, 4 * i + mi);
 }
 
 // ---- wide units: S = Q K^T of one m16 row tile over a step, in registers -------------
@@ -591,7 +597,7 @@ __device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32]) {
 // rescaling, and P as bf16 into this warp's 16 rows of the step's P tile (prow: the tile
 // row of row g; byte 2 tt of a row before the swizzle).  alpha / rescale report a moved
 // reference maximum: O, held in TMEM, is rescaled by the caller.
-template <int D, int NST>
+template <int D, int P, int NST>
 __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid, bool masked,
                                             const uint32_t (&qa)[D / 16][4],
                                             const uint32_t (&kw)[D / 32], float (&mref)[2],
@@ -611,7 +617,7 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb[nt >> 2] + kw[qd] + (nt & 3) * (8 * 128), b0, b1, b2, b3);
+      ldsm_x4(kb[nt >> 2] + kw[qd] + tok_off<D, P>(8 * (nt & 3)), b0, b1, b2, b3);
       mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
       mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
     }
@@ -911,17 +917,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < PPS; ++e) {
                 if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
-                  if (PPS == 1) {  // one box: both halves of the page
-                    tma_load_4d(kdst, &tm_k, &full[slot_s], 0, ids[e] * P, 0, head, pol);
-                    tma_load_4d(vdst, &tm_v, &full[slot_s], 0, ids[e] * P, 0, head, pol);
-                  } else {
-#pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                      const int off = h * kHalfBytes + e * P * 128;
-                      tma_load_4d(kdst + off, &tm_k, &full[slot_s], 0, ids[e] * P, h, head, pol);
-                      tma_load_4d(vdst + off, &tm_v, &full[slot_s], 0, ids[e] * P, h, head, pol);
-                    }
-                  }
+                  // One box per page and operand: [D/64 halves][P tokens][64].
+                  tma_load_4d(kdst + e * kPageBytes, &tm_k, &full[slot_s], 0, ids[e] * P, 0, head, pol);
+                  tma_load_4d(vdst + e * kPageBytes, &tm_v, &full[slot_s], 0, ids[e] * P, 0, head, pol);
                 }
               }
             }
@@ -998,11 +996,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot_s = st % kSlots;
             const int pg = it.page_begin + (2 * j + h) * PPS;
             const int loaded = min(PPS, it.page_end - pg) * P;
+            // V (MN-major): 64-column blocks a page half apart, 8-token groups 1024 B.
             const uint32_t v_lo = umma_desc_lo(
-                smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), kHalfBytes);
+                smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
             for (int kk = 0; kk < loaded / 16; ++kk)
               umma_bf16_lh(tmem + kTmemO, pb_lo + ((h * 64 + kk * 32) >> 4),
-                           v_lo + ((kk * 16 * 128) >> 4), kDescHi, kIdO, j > 0 || h > 0 || kk > 0);
+                           v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO,
+                           j > 0 || h > 0 || kk > 0);
             umma_commit(&empty[slot_s]);
           }
           umma_commit(&bo[b]);
@@ -1103,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qb[2 * kp + 1][nn][1]);
           }
         uint32_t koff[D / 16], voff[D / 16];
-        narrow_offsets<D>(lane, koff, voff);
+        narrow_offsets<D, P>(lane, koff, voff);
         float oT[D / 16][NN][4];
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt)
@@ -1140,16 +1140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* vrow = stages + slot_s * S::kStageBytes + S::kOperandBytes;
             const int z0 = max(0, L - t_abs0);
             for (int c = z0 * (D / 8) + lane; c < loaded * (D / 8); c += 32)
-              *reinterpret_cast<uint4*>(vrow + kv_off<D>(c / (D / 8), c % (D / 8))) =
+              *reinterpret_cast<uint4*>(vrow + kv_off<D, P>(c / (D / 8), c % (D / 8))) =
                   make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
             __syncwarp();
           }
           if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
-            narrow_stage<D, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+            narrow_stage<D, P, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
                                        lim, a.scale_log2, lane);
           else
-            narrow_stage<D, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
+            narrow_stage<D, P, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
                                       lim, a.scale_log2, lane);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot_s]);
@@ -1248,7 +1248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       uint32_t kw[D / 32];
-      wide_offsets<D>(lane, kw);
+      wide_offsets<D, P>(lane, kw);
       named_bar_sync(1, kConsumerThreads);  // the query staging becomes the P tiles
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
       float mref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
@@ -1278,7 +1278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* vt = stages + slot_s * S::kStageBytes + S::kOperandBytes;
             const int z0 = max(0, L - ta);
             for (int cc = z0 * (D / 8) + tid; cc < ld * (D / 8); cc += kConsumerThreads)
-              *reinterpret_cast<uint4*>(vt + kv_off<D>(cc / (D / 8), cc % (D / 8))) =
+              *reinterpret_cast<uint4*>(vt + kv_off<D, P>(cc / (D / 8), cc % (D / 8))) =
                   make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
           }
@@ -1304,10 +1304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float alpha[2];
           bool rescale;
           if (nst == 2)
-            wide_s_step<D, 2>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
+            wide_s_step<D, P, 2>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
                               limB, a.scale_log2, lane, prow);
           else
-            wide_s_step<D, 1>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
+            wide_s_step<D, P, 1>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
                               limB, a.scale_log2, lane, prow);
           if (__any_sync(0xffffffffu, rescale && sj > 0)) {
             // O holds the products up to the previous step: wait for the last of them,
@@ -1579,9 +1579,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // 4-D view of a page pool with the token before the column half:
 // (64, num_pages * P, D/64, Hkv), strides (Hkv*D*2, 128, D*2) bytes, 128-byte swizzle.
-// A box of (64, P, halves, 1) then lands as [half][token][64]: with 32-token pages one box
-// fills a whole stage operand ([D/64][32 tokens]); with 16-token pages each half of a page
-// is its own box.
+// A box of (64, P, D/64, 1) -- one page of one KV head -- then lands as
+// [half][token][64].
 bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d) {
   auto fn = get_encode_fn();
   if (!fn) return false;
@@ -1589,8 +1588,7 @@ bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d)
                               (cuuint64_t)d->head_dim / 64, (cuuint64_t)d->num_kv_heads};
   const cuuint64_t strides[3] = {(cuuint64_t)d->num_kv_heads * d->head_dim * 2, 128,
                                  (cuuint64_t)d->head_dim * 2};
-  const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size,
-                             d->page_size == 32 ? (cuuint32_t)d->head_dim / 64 : 1u, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)d->page_size, (cuuint32_t)d->head_dim / 64, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
