@@ -1695,7 +1695,9 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   pa.P = d.page_size;
   pa.maxp = d.max_pages_per_seq;
   pa.pps = kStageTokens / d.page_size;
-  pa.min_chunk = 4 * pa.pps;
+  // A split of fewer than 32 stages (1024 tokens) costs more in per-unit latency (query
+  // staging, the partial written and merged) than it returns in balance across SMs.
+  pa.min_chunk = 32 * pa.pps;
   pa.no_split = bf16 ? 0 : 1;
   pa.target_units = kUnitsPerSm * sms;
   pa.is_bf16 = bf16 ? 1 : 0;
