@@ -227,33 +227,11 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a 128-byte-swizzled operand tile (tile base 1024-
-// byte aligned).  K-major: rows of 128 bytes (64 bf16 of the contraction dimension),
-// 8-row groups `sbo` bytes apart; moving along the contraction dimension inside the
-// 128-byte row is done by adding its byte offset to the start address.  MN-major: the
-// 128-byte rows run along M or N, rows step along the contraction dimension, `lbo` is
-// the distance between 64-element column blocks and `sbo` between 8-row groups.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) /* descriptor version */ |
-         (2ull << 61) /* 128-byte swizzle */;
-}
-
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator;
 // a_mn / b_mn select the MN-major layout for that operand.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
 }
 
 // One arrival on `bar` once every tcgen05.mma this thread issued so far has completed.
@@ -327,35 +305,18 @@ __device__ __forceinline__ bool mbar_wait_fast(uint64_t* bar, uint32_t parity) {
   return mbar_test_wait(bar, parity) || mbar_wait(bar, parity);
 }
 
-// 8 / 16 consecutive TMEM columns of this thread's lane (warp-wide), then wait.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 }  // namespace vas
 
 namespace vas {
 
-// The two 32-bit halves of a 128-byte-swizzle descriptor: per-operand moves along a tile
-// change only the start address in the low word (`lo + (bytes >> 4)`).
+// The two 32-bit halves of the shared-memory matrix descriptor of a 128-byte-swizzled
+// operand tile (tile base 1024-byte aligned).  K-major: rows of 128 bytes (64 bf16 of
+// the contraction dimension), 8-row groups `sbo` bytes apart; a step along the
+// contraction dimension inside the 128-byte row is added to the start address.
+// MN-major: the 128-byte rows run along M or N and step along the contraction
+// dimension; `lbo` is the distance between 64-element column blocks, `sbo` between
+// 8-row groups.  Moves along a tile change only the start address in the low word
+// (`lo + (bytes >> 4)`).
 __device__ __forceinline__ uint32_t umma_desc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
@@ -363,6 +324,7 @@ __host__ __device__ constexpr uint32_t umma_desc_hi_sw128(uint32_t sbo) {
   return ((sbo >> 4) & 0x3FFFu) | (1u << 14) /* version */ | (2u << 29) /* 128-byte swizzle */;
 }
 
+// D[tmem] (+)= A[smem] * B[smem] (descriptors from their halves); issued by one thread.
 __device__ __forceinline__ void umma_bf16_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                              uint32_t hi, uint32_t idesc, bool accumulate) {
   asm volatile(
