@@ -14,20 +14,23 @@
 //   2. attn_bf16_kernel persistent, one CTA per SM, launched as a programmatic
 //                       dependent of the plan.  A producer warp takes work units (work
 //                       item x KV head) from an atomic counter and streams the unit's
-//                       K/V page slices into an 8-slot ring of 32-token stages with TMA
-//                       (one box per page and operand, landing as [half][token][64]
-//                       with the 128-byte swizzle), tracked by
-//                       mbarriers; it prefetches the next unit's descriptor and block-
-//                       table entries while streaming.  Four consumer warps compute on
-//                       the tensor cores (mma.sync m16n8k16, bf16 -> fp32):
+//                       K/V pages into an 8-slot ring of 32-token stages with TMA (one
+//                       box per page and operand, landing as [half][token][64] with the
+//                       128-byte swizzle), tracked by mbarriers; it prefetches the next
+//                       unit's descriptor and block-table entries while streaming.
+//                       Four consumer warps compute:
 //                         narrow units (<= 16 query rows per KV head: decode, small
-//                         verify groups) take S^T = K Q^T with the KV tokens as the
-//                         16-row M side and the GQA rows as N, so 8 rows fill an n8 tile;
-//                         P^T reaches the PV operand through movmatrix.  Each warp owns
-//                         whole stages (round robin) and keeps its own online softmax;
-//                         the four are merged at the end of the unit.
-//                         wide units (17..64 rows) take S = Q K^T with the rows as M
-//                         (m16 tiles spread over the warps) and P kept in registers.
+//                         verify groups) on warp MMA (mma.sync m16n8k16, bf16 -> fp32),
+//                         as S^T = K Q^T with the KV tokens as the 16-row M side and the
+//                         GQA rows as N, so 8 rows fill an n8 tile; P^T reaches the PV
+//                         operand through movmatrix.  Each warp owns whole stages (round
+//                         robin) and keeps its own online softmax; the four are merged
+//                         at the end of the unit.
+//                         wide units (17..64 rows): S = Q K^T with the rows as M on warp
+//                         MMA, two stages per step, softmax in registers, P as bf16 into
+//                         a shared tile; an MMA warp accumulates O += P V with tcgen05
+//                         (O in tensor memory, V read from the stage as the MN-major
+//                         operand), rescaled in place when a row's maximum moves.
 //                       A unit covering its whole sequence writes out/lse; otherwise it
 //                       writes a normalised fp32 partial and its lse, and the last split
 //                       to finish (atomic counter, no waiting) merges them by lse:
