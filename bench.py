@@ -251,14 +251,19 @@ def cpu_baseline(a, v, name):
 # ---------------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------------
-def dist_setup(args):
+def dist_setup(args, backend="nccl"):
+    """One process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE).  The path has no
+    data exchange: torch.distributed carries only the barrier and the max-over-ranks time."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+        else:
+            dist.init_process_group(backend)
     return world, rank, local
 
 
@@ -269,13 +274,21 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """The slowest rank's time (every rank returns it)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(bytes_per_rank_step, world, ms_per_step):
+    """Weak scaling: every rank streams its own batch, so the job moves world times the
+    per-rank bytes in the slowest rank's step time (GB/s)."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
 
 
 def run_ours(args):
@@ -405,13 +418,13 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier(world)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / K
-        e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": whole_job_rate(step_bytes, world, e2e_ms), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
 
     peak, peak_src = measured_peak()
     attn_gbs = a_bytes / (attn_ms * 1e-3) / 1e9
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_rate(step_bytes, world, ms_per_step)
     res = {
         "metric": METRIC,
         "value": value,
