@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged-attn achieved HBM GB/s (% of GB300 peak); spec-verify seqs/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def parse_args():
@@ -49,14 +50,16 @@ def parse_args():
     return ap.parse_args()
 
 
-def measured_peak():
+def measured_peak(key="hbm_gbs"):
+    """A denominator from MEASURED_PEAKS.json (`hbm_gbs` or `bf16_tflops`), else the
+    fallback figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return (FALLBACK_HBM_GBS if key == "hbm_gbs" else FALLBACK_BF16_TFLOPS), "fallback"
 
 
 # ---------------------------------------------------------------------------------
@@ -71,6 +74,16 @@ def attn_bytes(seq_lens, query_lens, Hq, Hkv, D, P, elem):
     bt = int(((L + P - 1) // P * 4).sum())
     lse = int((ql * Hq * 4).sum())
     return kv + qo + bt + lse
+
+
+def attn_flops(seq_lens, query_lens, Hq, D):
+    """Algorithmic flops: query row (token j, head h) of sequence i attends positions
+    0 .. L_i - ql_i + j, two products of 2 D flops per position."""
+    L = np.asarray(seq_lens, dtype=np.int64)
+    ql = np.asarray(query_lens, dtype=np.int64)
+    # sum over j < ql of (L - ql + j + 1) = ql (L - ql) + ql (ql + 1) / 2
+    pos = ql * (L - ql) + ql * (ql + 1) // 2
+    return int(pos.sum()) * Hq * 4 * D
 
 
 def verify_bytes(accepted_len, k, V):
@@ -424,6 +437,13 @@ def run_ours(args):
 
     peak, peak_src = measured_peak()
     attn_gbs = a_bytes / (attn_ms * 1e-3) / 1e9
+    a_flops = attn_flops(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
+                         a.head_dim)
+    attn_tflops = a_flops / (attn_ms * 1e-3) / 1e12
+    tpeak, tpeak_src = measured_peak("bf16_tflops")
+    # Above the ridge (peak flops / peak bytes) the call is bound by the tensor cores
+    # (chunked prefill); below it by HBM (decode and verify).
+    tensor_bound = a_flops / max(a_bytes, 1) > tpeak * 1e12 / (peak * 1e9)
     value = whole_job_rate(step_bytes, world, ms_per_step)
     res = {
         "metric": METRIC,
@@ -444,12 +464,18 @@ def run_ours(args):
                          % ((a.k_pages.numel() + a.v_pages.numel()) * elem / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "paged_attn": {"gbs": attn_gbs, "ms": attn_ms, "algorithmic_bytes": a_bytes,
+                       "algorithmic_flops": a_flops, "tflops": attn_tflops,
                        "frac_of_measured_peak": attn_gbs / peak,
                        "frac_of_nominal_8tbs": attn_gbs / NOMINAL_HBM_GBS},
-        "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": attn_gbs / peak, "traffic": ncu_traffic(name),
-                     "peak_source": peak_src,
-                     "kernel": "paged_attn_fwd (plan + attention with the fused LSE merge)"},
+        "roofline": ({"bound": "tensor", "achieved": attn_tflops, "peak": tpeak,
+                      "unit": "TFLOP/s", "frac": attn_tflops / tpeak, "traffic": ncu_traffic(name),
+                      "peak_source": tpeak_src + " (bf16, burst)",
+                      "kernel": "paged_attn_fwd (plan + attention with the fused LSE merge)"}
+                     if tensor_bound else
+                     {"bound": "hbm", "achieved": attn_gbs, "peak": peak, "unit": "GB/s",
+                      "frac": attn_gbs / peak, "traffic": ncu_traffic(name),
+                      "peak_source": peak_src,
+                      "kernel": "paged_attn_fwd (plan + attention with the fused LSE merge)"}),
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }

@@ -88,6 +88,26 @@ def subset_inputs(a: wl.AttentionInputs, seqs) -> wl.AttentionInputs:
                               a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype), np.concatenate(q_rows)
 
 
+def query_slice_inputs(a: wl.AttentionInputs, seq: int, j0: int, n: int):
+    """Query tokens j0 .. j0+n-1 of sequence `seq` as a problem of their own: context
+    L - ql + j0 + n (the same pages, so the same positions L - ql + j), query length n.
+    Returns (inputs on the CPU, the rows of the full problem they correspond to)."""
+    bt = a.block_table.cpu().numpy()
+    lens = a.seq_lens.cpu().numpy()
+    qlens = a.query_lens.cpu().numpy()
+    row0 = int(np.concatenate([[0], np.cumsum(qlens)])[seq])
+    L, ql, P = int(lens[seq]), int(qlens[seq]), a.page_size
+    Ls = L - ql + j0 + n
+    npg = (Ls + P - 1) // P
+    ids = torch.from_numpy(bt[seq, :npg].astype(np.int64)).to(a.k_pages.device)
+    rows = np.arange(row0 + j0, row0 + j0 + n)
+    sub = wl.AttentionInputs(a.q[torch.from_numpy(rows).to(a.q.device)].cpu(), a.k_pages[ids].cpu(),
+                             a.v_pages[ids].cpu(), torch.arange(npg, dtype=torch.int32)[None, :],
+                             torch.tensor([Ls], dtype=torch.int32), torch.tensor([n], dtype=torch.int32),
+                             a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
+    return sub, rows
+
+
 def compare_verify(acc, out, ref):
     """Bit-exact except sequences the oracle flags (a uniform within 1e-6 of its
     threshold): those must agree before the flagged position, and are counted.

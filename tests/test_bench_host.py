@@ -1,0 +1,28 @@
+"""Host-side counting in bench.py: algorithmic flops and bytes against brute force."""
+import os
+import sys
+
+import numpy as np
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_attn_flops_matches_a_per_row_count():
+    rng = np.random.default_rng(0)
+    L = rng.integers(1, 300, size=20)
+    ql = np.array([rng.integers(0, l + 1) for l in L])
+    Hq, D = 6, 64
+    brute = 0
+    for l, q in zip(L, ql):
+        for j in range(q):
+            brute += (l - q + j + 1) * Hq * 4 * D  # positions 0 .. L - ql + j
+    assert bench.attn_flops(L, ql, Hq, D) == brute
+
+
+def test_attn_bytes_counts_each_kv_element_once_per_kv_head():
+    # one sequence, L = 33 tokens, page 16: 3 block-table entries
+    got = bench.attn_bytes([33], [2], Hq=8, Hkv=2, D=64, P=16, elem=2)
+    kv = 33 * 2 * 64 * 2 * 2
+    qo = 2 * 8 * 64 * 2 * 2
+    assert got == kv + qo + 3 * 4 + 2 * 8 * 4

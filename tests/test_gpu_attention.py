@@ -7,8 +7,8 @@ import torch
 import oracle
 from verify_attention_spec_gb300 import workloads as wl
 
-from gpu_common import (compare_attention, oracle_attention, run_gpu_attention, subset_inputs,
-                        to_device)
+from gpu_common import (compare_attention, oracle_attention, query_slice_inputs,
+                        run_gpu_attention, subset_inputs, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -169,3 +169,29 @@ def test_query_rows_mismatch_total(vas_lib):
     assert torch.isnan(out[4:].float()).all()
     ref_o, ref_l = oracle_attention(a)
     compare_attention(out, lse, ref_o, ref_l, wl.BF16, rows=np.arange(4))
+
+
+def test_chunked_prefill_queries(vas_lib):
+    """Prompt chunks as queries: a 256-token chunk on 2048 of context, a whole 700-token
+    prompt (query length = context) and a 1024-token chunk, causal within each chunk;
+    GQA group 4, so up to 64 row blocks per KV head."""
+    a = _case([2048, 700, 1500], [256, 700, 1024], Hq=32, Hkv=8, D=128, P=16, seed=21)
+    ref_o, ref_l = oracle_attention(a)
+    out, lse = run_gpu_attention(vas_lib, to_device(a))
+    compare_attention(out, lse, ref_o, ref_l, wl.BF16)
+    assert vas_lib.vas_last_device_error() == 0
+
+
+def test_prefill8_sampled(vas_lib):
+    """The chunked-prefill workload (8 x 1024-token chunks on 4096 of context, 70B
+    shape) in full on the GPU; the oracle checks slices of it at their own positions:
+    the first and the last 64 query tokens of one chunk and 64 from the middle of
+    another."""
+    a = to_device(wl.workload_attention("prefill8", pool_device="cuda"))
+    out, lse = run_gpu_attention(vas_lib, a)
+    for seq, j0 in [(0, 0), (0, 960), (5, 500)]:
+        sub, rows = query_slice_inputs(a, seq, j0, 64)
+        ref_o, ref_l = oracle_attention(sub)
+        compare_attention(out, lse, ref_o, ref_l, wl.BF16, rows=rows)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    assert vas_lib.vas_last_device_error() == 0

@@ -24,6 +24,12 @@ Five workloads (named by what they are, counted from 0):
                   log-normal lengths (median 2048, sigma 1.2) clamped to [256, 32768];
                   448 decode + 64 verify with k=4; spec_verify over vocab 128256, seed 99.
 
+and one beyond them, for chunked prefill:
+
+* ``prefill8``  - 8 sequences of context 4096, each bringing a 1024-token prompt chunk
+                  (query length 1024, causal within the chunk), 70B attention shape,
+                  bf16, page 32; no spec_verify.
+
 Distributions (the pages leave them open; readings stated in the design doc): N(0, s) means
 standard deviation s; log-normal L = round(exp(ln median + sigma z)); Pareto
 L = floor(x_min (1 - U)^(-1/alpha)); uniform integers inclusive; p = softmax(logits),
@@ -78,6 +84,8 @@ WORKLOADS = {
                          272, 16, 7, 32000),
     "stress70b": Workload("stress70b", 99, 64, 8, 128, 32, BF16, "lognormal",
                           (2048.0, 1.2, 256, 32768), 512, 64, 4, 128256),
+    "prefill8": Workload("prefill8", 7, 64, 8, 128, 32, BF16, "fixed", (), 8, 0, 0, 0,
+                         fixed_lens=(4096,) * 8, fixed_qlens=(1024,) * 8),
 }
 ORDER = ["tiny", "decode64", "verify32", "mixed272", "stress70b"]
 
