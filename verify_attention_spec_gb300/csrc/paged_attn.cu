@@ -63,9 +63,16 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;      // TMA loads
 constexpr int kMmaWarp = kConsumerWarps + 1;       // tcgen05 issue for wide units
 constexpr int kThreads = kConsumerThreads + 64;    // + producer warp + MMA warp
-constexpr int kTmemCols = 128;                     // O of a wide unit: 128 lanes x D fp32
-constexpr int kTmemO = 0;
-constexpr int kRowBlock = 64;      // query rows per unit (four m16 tiles)
+constexpr int kTmemCols = 256;
+constexpr int kTmemS = 0;    // S of a prompt-chunk stage, two 32-column buffers
+constexpr int kTmemO = 64;   // O: 128 lanes x D fp32
+constexpr int kRowBlock = 64;      // query rows per unit (four m16 tiles) ...
+constexpr int kRowBlockTc = 128;   // ... or, for sequences with more rows (prompt chunks),
+                                   // 128: S and PV on tcgen05 with the rows in TMEM lanes
+// Rows per unit of a sequence with R query rows (G x query length).
+__host__ __device__ __forceinline__ int row_block(int R) {
+  return R > kRowBlock ? kRowBlockTc : kRowBlock;
+}
 // In a decode unit warp w consumes the stages s with s % kConsumerWarps == w and waits
 // on slot s % kSlots by phase parity.  The parity test is only sound if the slot's
 // previous fill was consumed by the same warp, i.e. if kSlots is a multiple of the
@@ -147,7 +154,7 @@ __device__ __forceinline__ SeqShape seq_shape(const PlanArgs& a, int32_t L, int3
   s.valid = ql >= 0 && ql <= a.T && L >= ql && (int64_t)L <= (int64_t)a.maxp * a.P;
   s.npages = s.valid ? (L + a.P - 1) / a.P : 0;
   s.R = s.valid ? a.G * ql : 0;
-  s.nrb = (s.R + kRowBlock - 1) / kRowBlock;
+  s.nrb = (s.R + row_block(s.R) - 1) / row_block(s.R);
   return s;
 }
 
@@ -417,15 +424,18 @@ struct Smem {
   // warps hold their query fragments.
   static constexpr int kPTileOff = 0;
   static constexpr int kPTileBytes = 128 * 128;
-  static constexpr int kWideBytes = kPTileOff + 2 * kPTileBytes;
+  // Prompt-chunk units: their query tile (128 rows, K-major 128-byte swizzle,
+  // [D/64][row][64]) after the P tiles.
+  static constexpr int kQTileOff = kPTileOff + 2 * kPTileBytes;
+  static constexpr int kWideBytes = kQTileOff + 128 * D * 2;
   static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
   static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
-  // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing], wide unit barriers
-  // bp[2], bo[2], bfin | meta[kSlots], flag[4], tmem base
-  static constexpr int kWideBars = 5;
+  // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing], tensor-memory unit
+  // barriers bp[2], bo[2], bs[2], bq, bfin | meta[kSlots], flag[4], tmem base
+  static constexpr int kWideBars = 8;
   static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars) * 8 + (kSlots + 4 + 1) * 4;
   static constexpr int kBytes = kBarOff + kBarBytes;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
@@ -790,11 +800,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kSlots;
   uint64_t* ufull = empty + kSlots;
   uint64_t* uempty = ufull + kRing;
-  // Wide units: bp[b] P of the stage with parity b is in shared memory; bo[b] the PV
-  // product of that stage is done; bfin every tcgen05.mma of the CTA has completed.
+  // Wide and prompt-chunk units: bp[b] P of the step with parity b is in shared memory;
+  // bo[b] the PV product of that step is done; bs[b] S of that step is in TMEM (prompt
+  // chunks); bq the query tile is staged (prompt chunks); bfin every tcgen05.mma of the
+  // CTA has completed.
   uint64_t* bp = uempty + kRing;
   uint64_t* bo = bp + 2;
-  uint64_t* bfin = bo + 2;
+  uint64_t* bs = bo + 2;
+  uint64_t* bq = bs + 2;
+  uint64_t* bfin = bq + 1;
   int32_t* meta = reinterpret_cast<int32_t*>(bfin + 1);
   int32_t* flag = meta + kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flag + 4);
@@ -812,7 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bp[b], kConsumerWarps);
       mbar_init(&bo[b], 1);
+      mbar_init(&bs[b], 1);
     }
+    mbar_init(bq, kConsumerWarps);
     mbar_init(bfin, 1);
     mbar_fence_init();
   }
@@ -957,13 +973,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lanes, N = D, 16 tokens per product over the step's loaded tokens) and commits
     // to the stages' empty barriers (they may be refilled) and to bo[b].  Lane 0
     // issues; the warp waits together.
-    uint32_t stage_it = 0, unit_it = 0, wk = 0;
+    // wk: steps of wide and prompt-chunk units (bp, bo); wc: stages of prompt-chunk units
+    // (bs, the S buffers); wq: prompt-chunk units (bq).
+    uint32_t stage_it = 0, unit_it = 0, wk = 0, wc = 0, wq = 0;
     bool ok = true;
     constexpr uint32_t kIdO = umma_idesc_bf16(128, D, false, true);
+    constexpr uint32_t kIdS = umma_idesc_bf16(128, P == 32 ? 32 : 16, false, false);
     // All operands are 128-byte swizzled with 1024-byte 8-row groups: the high descriptor
     // word is shared, the low word carries the start address.
     constexpr uint32_t kDescHi = umma_desc_hi_sw128(1024);
     const uint32_t p_lo = umma_desc_lo(smem_u32(scratch + S::kPTileOff), 16);  // P tile 0
+    const uint32_t q_lo = umma_desc_lo(smem_u32(scratch + S::kQTileOff), 16);
     for (;;) {
       const int slot = unit_it % kRing;
       if (!mbar_wait(&ufull[slot], (unit_it / kRing) & 1)) {
@@ -979,9 +999,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.seq < 0) continue;
       const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
       const int R = a.G * re.sp.qlen;
-      const int Rb = min(kRowBlock, R - (it.split_rb & ((1 << kRbBits) - 1)) * kRowBlock);
-      if (Rb <= kNarrowRows || n_stages == 0) {  // consumed by the consumer warps alone
+      const int RB = row_block(R);
+      const int Rb = min(RB, R - (it.split_rb & ((1 << kRbBits) - 1)) * RB);
+      if (n_stages == 0 || (RB == kRowBlock && Rb <= kNarrowRows)) {  // consumer warps alone
         stage_it += n_stages;
+        continue;
+      }
+      if (RB == kRowBlockTc) {
+        // A prompt-chunk unit, one step per stage.  S_k = Q K_k^T into S buffer k & 1
+        // (M 128 lanes; N the stage's 32 tokens, as two 16-token products with 16-token
+        // pages) once the query tile is staged and the stage has landed; O += P_k V_k
+        // after bp.  S of stage k + 2 is issued after O of stage k, so its completion also
+        // covers that product, the last reader of the P tile stage k + 2 rewrites.
+        if (!mbar_wait(bq, wq & 1)) {
+          ok = false;
+          break;
+        }
+        ++wq;
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t st = stage_it + j;
+          const int slot_s = st % kSlots;
+          if (!mbar_wait(&full[slot_s], (st / kSlots) & 1)) return false;
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t k_lo = umma_desc_lo(smem_u32(stages + slot_s * S::kStageBytes), 16);
+            const uint32_t dt = tmem + kTmemS + ((wc + j) & 1) * 32;
+            const int pg = it.page_begin + j * PPS;
+            const int n_in = min(PPS, it.page_end - pg);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t qstep = ((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4;
+              for (int e = 0; e < n_in; ++e) {
+                const uint32_t kstep = (e * kPageBytes + (ks >> 2) * (P * 128) + (ks & 3) * 32) >> 4;
+                umma_bf16_lh(dt + e * P, q_lo + qstep, k_lo + kstep, kDescHi, kIdS, ks > 0);
+              }
+            }
+            umma_commit(&bs[(wc + j) & 1]);
+          }
+          __syncwarp();
+          return true;
+        };
+        ok = issue_s(0) && (n_stages < 2 || issue_s(1));
+        for (int j = 0; ok && j < n_stages; ++j) {
+          const uint32_t k = wk + j, b = k & 1;
+          if (!mbar_wait(&bp[b], (k >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t st = stage_it + j;
+            const int slot_s = st % kSlots;
+            const int pg = it.page_begin + j * PPS;
+            const int loaded = min(PPS, it.page_end - pg) * P;
+            const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
+            const uint32_t v_lo = umma_desc_lo(
+                smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
+            for (int kk = 0; kk < loaded / 16; ++kk)
+              umma_bf16_lh(tmem + kTmemO, pb_lo + ((kk * 32) >> 4), v_lo + (tok_off<D, P>(16 * kk) >> 4),
+                           kDescHi, kIdO, j > 0 || kk > 0);
+            umma_commit(&empty[slot_s]);
+            umma_commit(&bo[b]);
+          }
+          __syncwarp();
+          if (j + 2 < n_stages) ok = issue_s(j + 2);
+        }
+        wk += n_stages;
+        wc += n_stages;
+        stage_it += n_stages;
+        if (!ok) break;
         continue;
       }
       const int n_steps = (n_stages + 1) >> 1;
@@ -1031,7 +1117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = lane >> 2, tq = lane & 3;
   const float kLn2 = 0.6931471805599453f;
   uint32_t stage_it = 0, unit_it = 0;
-  uint32_t wk = 0;  // stages of wide units so far (the MMA warp counts the same)
+  uint32_t wk = 0;  // steps of wide and prompt-chunk units (the MMA warp counts the same)
+  uint32_t wc = 0;  // stages of prompt-chunk units (S buffers, bs)
   bool timed_out = false;
   PendingMerge pm;
   pm.valid = 0;
@@ -1066,14 +1153,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int split = it.split_rb >> kRbBits, rb = it.split_rb & ((1 << kRbBits) - 1);
     const int L = sp.len, ql = sp.qlen;
     const int R = a.G * ql;
-    const int r0 = rb * kRowBlock;
-    const int Rb = min(kRowBlock, R - r0);
+    const int RB = row_block(R);
+    const int r0 = rb * RB;
+    const int Rb = min(RB, R - r0);
     const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
     const uint32_t stage0 = stage_it;  // first stage of this unit in the CTA's stream
     const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
 
-    const bool wide = Rb > kNarrowRows && n_stages > 0;
-    {
+    const bool chunk = RB == kRowBlockTc && n_stages > 0;  // prompt chunk: tcgen05 S and PV
+    const bool wide = !chunk && Rb > kNarrowRows && n_stages > 0;
+    if (chunk) {
+      // The query tile for tcgen05 S: rows 0 .. Rb-1 (row r: token r / G, head
+      // head * G + r % G) in the K-major 128-byte-swizzled layout.  Rows past Rb keep
+      // whatever they held: they only feed accumulator rows that are never read.
+      constexpr int kChunks = D / 8;
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+      uint8_t* qt = scratch + S::kQTileOff;
+      for (int c = tid; c < Rb * kChunks; c += kConsumerThreads) {
+        const int row = c / kChunks, gc = c % kChunks;
+        *reinterpret_cast<uint4*>(qt + (gc >> 3) * (128 * 128) + row * 128 +
+                                  (((gc & 7) ^ (row & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(qg + out_row(a, sp, head, r0 + row) * D + gc * 8);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bq);
+    } else {
       // Stage the unit's query rows (row r: token r / G, head head * G + r % G); rows
       // past Rb up to the MMA tile are zero.
       constexpr int kChunks = D / 8;
@@ -1090,7 +1195,156 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     bool poison = false;
-    if (!wide) {
+    if (chunk) {
+      // ========================= prompt-chunk unit (tcgen05) =========================
+      // Thread r of the consumer warps owns row r of the 128-row block (TMEM lane r).  Per
+      // stage it reads its 32 scores from TMEM, applies the causal limit and the online
+      // softmax, and writes its probabilities as bf16 into the stage's P tile; the MMA
+      // warp accumulates O = P V in TMEM, rescaled here in place when the reference
+      // maximum moves.
+      const int r = tid;
+      const bool row_ok = r < Rb;
+      const bool warp_ok = 32 * warp < Rb;
+      const int lim = row_ok ? L - ql + (r0 + r) / a.G : -1;
+      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+      const float c = a.scale_log2;
+      float mref = -INFINITY, l = 0.f;
+      for (int si = 0; si < n_stages; ++si, ++stage_it) {
+        const uint32_t k = wk + si, b = k & 1, kc = wc + si;
+        const int slot_s = stage_it % kSlots;
+        // S of this stage is in TMEM; its commit also covers the product that last read
+        // P tile b.
+        const bool got = mbar_wait_fast(&bs[kc & 1], (kc >> 1) & 1) &&
+                         mbar_wait_fast(&full[slot_s], (stage_it / kSlots) & 1);
+        if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
+          timed_out = true;
+          stage_it += n_stages - si;
+          break;
+        }
+        tc_fence_after();
+        if (meta[slot_s]) poison = true;
+        const int pg = it.page_begin + si * PPS;
+        const int loaded = min(PPS, it.page_end - pg) * P;
+        const int t_abs0 = pg * P;
+        if (t_abs0 + loaded > L) {
+          // Slots past the sequence end may hold anything (NaN included); their V rows
+          // meet P = 0 in the product, so they are zeroed first.
+          uint8_t* vt = stages + slot_s * S::kStageBytes + S::kOperandBytes;
+          const int z0 = max(0, L - t_abs0);
+          for (int cc = z0 * (D / 8) + tid; cc < loaded * (D / 8); cc += kConsumerThreads)
+            *reinterpret_cast<uint4*>(vt + kv_off<D, P>(cc / (D / 8), cc % (D / 8))) =
+                make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();
+        }
+        if (warp_ok) {
+          uint32_t sr[32];
+          tmem_ld32(tmem + lane_base + kTmemS + (kc & 1) * 32, sr);
+          // Valid tokens of this row form a prefix of the stage: i < loaded, t <= lim.
+          const int nv = row_ok ? max(0, min(loaded, lim - t_abs0 + 1)) : 0;
+          const uint32_t valid = nv >= 32 ? 0xffffffffu : (1u << nv) - 1u;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            m4[i & 3] = fmaxf(m4[i & 3], (valid >> i) & 1 ? __uint_as_float(sr[i]) : -INFINITY);
+          const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c;  // c > 0
+          const bool rebase = mx > mref + kRebase;
+          const bool rescale = rebase && si > 0 && mref != -INFINITY;
+          const float alpha = rebase ? exp2f(mref - mx) : 1.f;
+          if (rebase) {
+            l *= alpha;
+            mref = mx;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O holds the products up to the previous stage: wait for the last of them.
+            const uint32_t kp = k - 1;
+            if (!mbar_wait(&bo[kp & 1], (kp >> 1) & 1)) timed_out = true;
+            tc_fence_after();
+            const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t ov[32];
+              tmem_ld32(tmem + lane_base + kTmemO + cc * 32, ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+              tmem_st32(tmem + lane_base + kTmemO + cc * 32, ov);
+            }
+          }
+          const float mu = mref == -INFINITY ? 0.f : mref;
+          uint32_t pw[16];
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float e0 = ex2_approx(fmaf(__uint_as_float(sr[i]), c, -mu));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(sr[i + 1]), c, -mu));
+            const float p0 = (valid >> i) & 1 ? e0 : 0.f;
+            const float p1 = (valid >> (i + 1)) & 1 ? e1 : 0.f;
+            s4[(i >> 1) & 3] += p0 + p1;
+            pw[i >> 1] = pack_bf16x2(p0, p1);
+          }
+          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          uint8_t* prow = scratch + S::kPTileOff + b * S::kPTileBytes + r * 128;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+                make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bp[b]);
+      }
+      // The unit's last product (it covers every earlier one).
+      if (!timed_out) {
+        const uint32_t kl = wk + n_stages - 1;
+        if (!mbar_wait(&bo[kl & 1], (kl >> 1) & 1)) timed_out = true;
+      }
+      wk += n_stages;
+      wc += n_stages;
+      tc_fence_after();
+      poison = named_bar_or(1, kConsumerThreads, poison);
+      if (named_bar_or(1, kConsumerThreads, timed_out)) {
+        timed_out = true;
+        break;
+      }
+      if (warp_ok) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float row_lse = l > 0.f ? (mref + log2f(l)) * kLn2 : -INFINITY;
+        if (poison) row_lse = NAN;
+        const bool whole = sp.nsplit == 1;
+        const size_t orow = row_ok ? (whole ? out_row(a, sp, head, r0 + r)
+                                            : partial_row(a, sp, split, head, r0 + r))
+                                   : 0;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_base + kTmemO + cc * 32, ov);
+          if (!row_ok) continue;
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = poison ? NAN : __uint_as_float(ov[i]) * inv;
+          if (whole) {
+            uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * D +
+                                                 cc * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              og[q4] = make_uint4(pack_bf16x2(x[8 * q4], x[8 * q4 + 1]),
+                                  pack_bf16x2(x[8 * q4 + 2], x[8 * q4 + 3]),
+                                  pack_bf16x2(x[8 * q4 + 4], x[8 * q4 + 5]),
+                                  pack_bf16x2(x[8 * q4 + 6], x[8 * q4 + 7]));
+          } else {
+            float4* po = reinterpret_cast<float4*>(a.part_o + orow * D + cc * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              po[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+          }
+        }
+        if (row_ok) {
+          if (whole) a.lse[orow] = row_lse;
+          else a.part_lse[orow] = row_lse;
+        }
+      }
+      tc_fence_before();
+    } else if (!wide) {
       // ============================ narrow unit ============================
       auto run = [&](auto nn_tag) {
         constexpr int NN = decltype(nn_tag)::value;
@@ -1435,7 +1689,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
     const int rb = it.split_rb & ((1 << kRbBits) - 1);
     const int L = sp.len, ql = sp.qlen, R = a.G * ql;
     const int32_t* bt_row = a.block_table + (size_t)it.seq * a.maxp;
-    for (int r = rb * kRowBlock + warp; r < min(R, rb * kRowBlock + kRowBlock); r += 4) {
+    const int RB = row_block(R);
+    for (int r = rb * RB + warp; r < min(R, rb * RB + RB); r += 4) {
       const int j = r / a.G;
       const int pos = L - ql + j;
       const size_t orow = out_row(a, sp, head, r);
