@@ -56,6 +56,9 @@ def _load():
     lib.oracle_paged_attn.argtypes = [P, P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32,
                                       i32, dbl, P, P]
     lib.oracle_paged_attn.restype = i32
+    lib.oracle_paged_attn_tree.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32,
+                                           i32, i32, dbl, P, P]
+    lib.oracle_paged_attn_tree.restype = i32
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox4x32_10_many.argtypes = [P, i64, P, P]
@@ -90,11 +93,13 @@ def _as_storage(x: np.ndarray, dtype_code: int) -> np.ndarray:
 
 
 def paged_attn(q, k_pages, v_pages, block_table, seq_lens, query_lens, *, dtype_code: int,
-               scale: float | None = None):
-    """Float64 paged attention (oracle.c: oracle_paged_attn).
+               scale: float | None = None, parents=None):
+    """Float64 paged attention (oracle.c: oracle_paged_attn, oracle_paged_attn_tree).
 
     q: [total_q_tokens, Hq, D]; k_pages/v_pages: [num_pages, page_size, Hkv, D], given as
     float32, raw bf16 bits (uint16) or float64 according to ``dtype_code``.
+    parents: optional int32 [total_q_tokens], a draft tree (each query token's parent
+    among its sequence's query tokens, -1 for a root); None is the causal window.
     Returns (out float64 [total_q_tokens, Hq, D], lse float64 [total_q_tokens, Hq]).
     """
     lib = _load()
@@ -113,9 +118,17 @@ def paged_attn(q, k_pages, v_pages, block_table, seq_lens, query_lens, *, dtype_
         scale = 1.0 / np.sqrt(D)
     out = np.zeros((T, Hq, D), dtype=np.float64)
     lse = np.zeros((T, Hq), dtype=np.float64)
-    rc = lib.oracle_paged_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), dtype_code, _ptr(bt),
-                               _ptr(sl), _ptr(ql), B, Hq, Hkv, D, page_size, num_pages, maxp,
-                               float(scale), _ptr(out), _ptr(lse))
+    if parents is None:
+        rc = lib.oracle_paged_attn(_ptr(q), _ptr(k_pages), _ptr(v_pages), dtype_code, _ptr(bt),
+                                   _ptr(sl), _ptr(ql), B, Hq, Hkv, D, page_size, num_pages,
+                                   maxp, float(scale), _ptr(out), _ptr(lse))
+    else:
+        par = np.ascontiguousarray(parents, dtype=np.int32)
+        assert par.shape == (T,)
+        rc = lib.oracle_paged_attn_tree(_ptr(q), _ptr(k_pages), _ptr(v_pages), dtype_code,
+                                        _ptr(bt), _ptr(sl), _ptr(ql), _ptr(par), B, Hq, Hkv, D,
+                                        page_size, num_pages, maxp, float(scale), _ptr(out),
+                                        _ptr(lse))
     if rc != OK:
         raise ValueError(f"oracle_paged_attn rejected its arguments (code {rc})")
     return out, lse

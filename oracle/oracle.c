@@ -92,16 +92,24 @@ static double load_elem(const void* base, int dtype, size_t idx) {
  *
  * q and out are [total_q_tokens, num_q_heads, head_dim], rows packed by sequence in
  * order; lse is [total_q_tokens, num_q_heads].  For every query row:
- *     s_t   = scale * <q, k_t>          for t = 0 .. pos
+ *     s_t   = scale * <q, k_t>          for the visible positions t
  *     lse   = log sum_t exp(s_t)
  *     out   = sum_t exp(s_t - lse) v_t
+ * Query token j of a sequence with context L and ql query tokens sits at position
+ * L - ql + j.  Without a tree it sees positions 0 .. L - ql + j (causal within the
+ * draft window).  With a draft tree (neuralmasteryai.com, "Tree Attention & Medusa
+ * Heads": candidate paths verified in one pass), parents[row] is the index of the
+ * token's parent among its sequence's query tokens (-1: the root, attached to the
+ * context), and the token sees the context 0 .. L - ql - 1 and the positions of
+ * its ancestors and itself.  A parent must come before its child.
  * Returns ORC_OK, or a negative code for arguments that make the result undefined.
  * ---------------------------------------------------------------------------- */
-int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, int dtype,
-                      const int32_t* block_table, const int32_t* seq_lens,
-                      const int32_t* query_lens, int num_seqs, int num_q_heads,
-                      int num_kv_heads, int head_dim, int page_size, int num_pages,
-                      int max_pages_per_seq, double scale, double* out, double* lse) {
+static int paged_attn_impl(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const int32_t* query_lens, const int32_t* parents, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                           int num_pages, int max_pages_per_seq, double scale, double* out,
+                           double* lse) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       page_size <= 0 || num_pages < 0 || max_pages_per_seq < 0)
     return ORC_E_ARG;
@@ -128,6 +136,16 @@ int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, i
     }
     row0[i + 1] = row0[i] + ql;
   }
+  if (parents) {
+    for (int i = 0; i < num_seqs; ++i)
+      for (int j = 0; j < query_lens[i]; ++j) {
+        const int32_t pj = parents[row0[i] + j];
+        if (pj < -1 || pj >= j) {
+          free(row0);
+          return ORC_E_ARG;
+        }
+      }
+  }
 
   const int group = num_q_heads / num_kv_heads;
   const int64_t work = (int64_t)num_seqs * num_q_heads;
@@ -141,12 +159,18 @@ int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, i
     const int ql = query_lens[i];
     if (ql == 0) continue;
     double* s = (double*)malloc(sizeof(double) * (size_t)L);
+    char* vis = (char*)malloc((size_t)L + 1);
     for (int j = 0; j < ql; ++j) {
       const int pos = L - ql + j; /* absolute position of this query token */
       const int64_t row = row0[i] + j;
       const size_t qbase = ((size_t)row * num_q_heads + h) * head_dim;
+      /* visible positions */
+      for (int t = 0; t <= pos; ++t) vis[t] = !parents || t < L - ql;
+      if (parents)
+        for (int a = j; a >= 0; a = parents[row0[i] + a]) vis[L - ql + a] = 1;
       double m = -INFINITY;
       for (int t = 0; t <= pos; ++t) {
+        if (!vis[t]) continue;
         const int32_t page = block_table[(size_t)i * max_pages_per_seq + t / page_size];
         const int slot = t % page_size;
         const size_t kbase =
@@ -158,12 +182,14 @@ int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, i
         if (s[t] > m) m = s[t];
       }
       double sum = 0.0;
-      for (int t = 0; t <= pos; ++t) sum += exp(s[t] - m);
+      for (int t = 0; t <= pos; ++t)
+        if (vis[t]) sum += exp(s[t] - m);
       const double row_lse = m + log(sum);
       lse[(size_t)row * num_q_heads + h] = row_lse;
       double* o = out + qbase;
       for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
       for (int t = 0; t <= pos; ++t) {
+        if (!vis[t]) continue;
         const double wt = exp(s[t] - row_lse);
         const int32_t page = block_table[(size_t)i * max_pages_per_seq + t / page_size];
         const int slot = t % page_size;
@@ -172,10 +198,34 @@ int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, i
         for (int d = 0; d < head_dim; ++d) o[d] += wt * load_elem(v_pages, dtype, vbase + d);
       }
     }
+    free(vis);
     free(s);
   }
   free(row0);
   return ORC_OK;
+}
+
+int oracle_paged_attn(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                      const int32_t* block_table, const int32_t* seq_lens,
+                      const int32_t* query_lens, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int page_size, int num_pages,
+                      int max_pages_per_seq, double scale, double* out, double* lse) {
+  return paged_attn_impl(q, k_pages, v_pages, dtype, block_table, seq_lens, query_lens, NULL,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                         max_pages_per_seq, scale, out, lse);
+}
+
+/* The same with a draft tree: parents[total_q_tokens] as described above. */
+int oracle_paged_attn_tree(const void* q, const void* k_pages, const void* v_pages, int dtype,
+                           const int32_t* block_table, const int32_t* seq_lens,
+                           const int32_t* query_lens, const int32_t* parents, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                           int num_pages, int max_pages_per_seq, double scale, double* out,
+                           double* lse) {
+  if (!parents) return ORC_E_ARG;
+  return paged_attn_impl(q, k_pages, v_pages, dtype, block_table, seq_lens, query_lens, parents,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
+                         max_pages_per_seq, scale, out, lse);
 }
 
 /* ------------------------------------------------------------------------------

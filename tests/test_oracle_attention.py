@@ -195,3 +195,84 @@ def test_rejects_bad_page_and_lengths():
         oracle.paged_attn(qs[0], kp, vp, bad, [20], [1], dtype_code=oracle.F64)
     with pytest.raises(ValueError):
         oracle.paged_attn(np.zeros((21, 2, 8)), kp, vp, bt, [20], [21], dtype_code=oracle.F64)
+
+
+# ---- draft trees ("Tree Attention & Medusa Heads" on the neuralmasteryai.com page) -----
+def _tree_case(rng, L, ql, Hq=4, Hkv=2, D=16, P=8):
+    k = rng.standard_normal((L, Hkv, D))
+    v = rng.standard_normal((L, Hkv, D))
+    q = rng.standard_normal((ql, Hq, D))
+    kp, vp, bt = scatter_to_pool([k], [v], P, (L + P - 1) // P + 2, rng)
+    return q, k, v, kp, vp, bt
+
+
+def test_tree_chain_is_the_causal_window():
+    rng = np.random.default_rng(40)
+    L, ql = 37, 6
+    q, k, v, kp, vp, bt = _tree_case(rng, L, ql)
+    args = (q, kp, vp, bt, np.array([L]), np.array([ql]))
+    o_c, l_c = oracle.paged_attn(*args, dtype_code=oracle.F64)
+    o_t, l_t = oracle.paged_attn(*args, dtype_code=oracle.F64,
+                                 parents=np.arange(ql, dtype=np.int32) - 1)
+    np.testing.assert_array_equal(o_t, o_c)
+    np.testing.assert_array_equal(l_t, l_c)
+
+
+def test_tree_node_is_decode_over_its_path():
+    """Each node of a random tree sees the context and its root-to-node path: the same as
+    one decode query over a sequence made of exactly those tokens, in order, placed in a
+    fresh paged pool (the causal oracle, pinned above)."""
+    rng = np.random.default_rng(41)
+    L, ql, P = 45, 9, 8
+    Hq, Hkv, D = 4, 2, 16
+    q, k, v, kp, vp, bt = _tree_case(rng, L, ql, Hq, Hkv, D, P)
+    parents = np.array([-1] + [int(rng.integers(-1, j)) for j in range(1, ql)], dtype=np.int32)
+    parents[3] = -1  # at least two roots
+    o_t, l_t = oracle.paged_attn(q, kp, vp, bt, np.array([L]), np.array([ql]),
+                                 dtype_code=oracle.F64, parents=parents)
+    ctx = L - ql
+    for j in range(ql):
+        path, a = [], j
+        while a >= 0:
+            path.append(a)
+            a = parents[a]
+        toks = list(range(ctx)) + [ctx + a for a in reversed(path)]
+        kp2, vp2, bt2 = scatter_to_pool([k[toks]], [v[toks]], P,
+                                        (len(toks) + P - 1) // P + 1, rng)
+        o_d, l_d = oracle.paged_attn(q[j:j + 1], kp2, vp2, bt2, np.array([len(toks)]),
+                                     np.array([1]), dtype_code=oracle.F64)
+        np.testing.assert_allclose(o_t[j], o_d[0], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l_t[j], l_d[0], rtol=0, atol=1e-12)
+
+
+def test_tree_parent_after_child_is_rejected():
+    rng = np.random.default_rng(42)
+    q, k, v, kp, vp, bt = _tree_case(rng, 20, 4)
+    with pytest.raises(ValueError):
+        oracle.paged_attn(q, kp, vp, bt, np.array([20]), np.array([4]), dtype_code=oracle.F64,
+                          parents=np.array([-1, 0, 3, 1], dtype=np.int32))
+
+
+def test_tree_batched_sequences_match_alone():
+    """Two sequences with their own trees in one call give what each gives alone (the
+    parents index the sequence's own query tokens)."""
+    rng = np.random.default_rng(43)
+    P, Hq, Hkv, D = 8, 4, 2, 16
+    L = [30, 26]
+    ql = [5, 7]
+    par = [np.array([-1, 0, 0, 1, -1], dtype=np.int32),
+           np.array([-1, 0, 1, 1, 3, -1, 5], dtype=np.int32)]
+    ks = [rng.standard_normal((l, Hkv, D)) for l in L]
+    vs = [rng.standard_normal((l, Hkv, D)) for l in L]
+    qs = [rng.standard_normal((n, Hq, D)) for n in ql]
+    kp, vp, bt = scatter_to_pool(ks, vs, P, sum((l + P - 1) // P for l in L) + 2, rng)
+    o, l = oracle.paged_attn(np.concatenate(qs), kp, vp, bt, np.array(L), np.array(ql),
+                             dtype_code=oracle.F64, parents=np.concatenate(par))
+    r = 0
+    for i in range(2):
+        kp1, vp1, bt1 = scatter_to_pool([ks[i]], [vs[i]], P, (L[i] + P - 1) // P, rng)
+        o1, l1 = oracle.paged_attn(qs[i], kp1, vp1, bt1, np.array([L[i]]), np.array([ql[i]]),
+                                   dtype_code=oracle.F64, parents=par[i])
+        np.testing.assert_array_equal(o[r:r + ql[i]], o1)
+        np.testing.assert_array_equal(l[r:r + ql[i]], l1)
+        r += ql[i]
