@@ -129,6 +129,32 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
                    const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
                    vas_stream_t stream);
 
+/* paged_attn_fwd for draft trees.
+ *
+ * Defined by: "Continuous Batching & Speculative Decoding" (neuralmasteryai.com),
+ * section "4. Tree Attention & Medusa Heads" -- the draft is a tree of candidate
+ * tokens, verified in one pass under a tree attention mask; and
+ * "llm-inference-optimization-batching" (tempatgunting.com), section "Draft Model
+ * Selection and Tree-Style Variants" -- the verification mask becomes a tree mask.
+ *
+ * tree_mask   [T] device uint64, 8-byte aligned, one word per query token (the rows of
+ *             q).  For query token j of sequence i, bit a (a < j) set means draft token a
+ *             of the same sequence (position L_i - ql_i + a) is an ancestor of j in the
+ *             tree.  Token j then attends to every context position (0 .. L_i - ql_i - 1),
+ *             to the draft tokens whose bits are set, and to itself (its own bit is
+ *             implied).  Bits a >= j are ignored: a parent precedes its children in the
+ *             packing, so a chain (bits 0 .. j-1 set) is exactly paged_attn_fwd.
+ *             Sequences with ql_i == 1 or ql_i > 64 ignore their words and use the
+ *             causal window of paged_attn_fwd (64 draft tokens at most per tree).
+ * Other arguments, results and errors: those of paged_attn_fwd; a null tree_mask is
+ * VAS_E_INVALID_ARG.
+ */
+int paged_attn_fwd_tree(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        const int32_t* query_lens, const uint64_t* tree_mask, void* out,
+                        float* lse, const vas_attn_dims* dims, void* workspace,
+                        size_t workspace_bytes, vas_stream_t stream);
+
 /* paged_attn_fwd without a workspace argument, for callers that cannot allocate device
  * memory: code being captured into a CUDA graph (where cudaMalloc is not allowed), hosts
  * that hand a plug-in only the tensors of a call, or callers whose allocator is out of

@@ -18,7 +18,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["paged_attn_fwd", "paged_attn_workspace_size", "spec_verify", "vas_last_device_error",
+    for n in ["paged_attn_fwd", "paged_attn_fwd_tree", "paged_attn_workspace_size", "spec_verify", "vas_last_device_error",
               "vas_pool_create", "vas_build_block_table", "vas_seq_rollback"]:
         assert n in names
 
@@ -73,6 +73,16 @@ def test_host_validation_without_launch(vas_lib):
     # empty batch is a no-op
     assert lib.paged_attn_fwd(null, null, null, null, null, null, null, null,
                               ctypes.byref(_dims(vas_lib, num_seqs=0)), null, 0, null) == vas_lib.VAS_OK
+    # the draft-tree entry point: a null or misaligned mask is refused on the host
+    st = lib.paged_attn_fwd_tree(fake, fake, fake, fake, fake, fake, null, fake, fake,
+                                 ctypes.byref(d), fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG
+    st = lib.paged_attn_fwd_tree(fake, fake, fake, fake, fake, fake, P((1 << 20) + 4), fake, fake,
+                                 ctypes.byref(d), fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG
+    st = lib.paged_attn_fwd_tree(fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                 ctypes.byref(d), fake, 16, null)
+    assert st == vas_lib.VAS_E_WORKSPACE
     # spec_verify argument checks
     assert lib.spec_verify(fake, fake, fake, 1, fake, fake, 4, 3, 0, null) == vas_lib.VAS_E_INVALID_ARG
     assert lib.spec_verify(null, fake, fake, 1, fake, fake, 4, 3, 10, null) == vas_lib.VAS_E_INVALID_ARG

@@ -59,6 +59,7 @@ _sig = {
     "paged_attn_workspace_size": ([_P_dims], _sz),
     "paged_attn_workspace_min": ([_P_dims], _sz),
     "paged_attn_fwd": ([_c_void_p] * 8 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
+    "paged_attn_fwd_tree": ([_c_void_p] * 9 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
     "spec_verify": ([_c_void_p, _c_void_p, _c_void_p, _u64, _c_void_p, _c_void_p, _i32, _i32, _i32,
                      _c_void_p], ctypes.c_int),
     "vas_last_device_error": ([ctypes.POINTER(_i32), _c_void_p], ctypes.c_int),
@@ -159,6 +160,27 @@ def paged_attn_fwd(q, k_pages, v_pages, block_table, seq_lens, query_lens, out, 
         _dev(lse, "lse", torch.float32), ctypes.byref(dims), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     _check("paged_attn_fwd", st)
+
+
+def paged_attn_fwd_tree(q, k_pages, v_pages, block_table, seq_lens, query_lens, tree_mask, out,
+                        lse, workspace, *, scale: float = 0.0, dims: Optional[vas_attn_dims] = None,
+                        stream=None) -> None:
+    """Draft-tree attention (include/vas.h: paged_attn_fwd_tree).  tree_mask [T] int64 (the
+    bits of a uint64 per query token: its ancestors among its sequence's draft tokens)."""
+    if dims is None:
+        dims = attn_dims(q, k_pages, block_table, seq_lens, scale)
+    if tree_mask.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)):
+        raise ValueError("tree_mask must be a 64-bit integer tensor")
+    if tree_mask.numel() != q.shape[0]:
+        raise ValueError("tree_mask needs one word per query token")
+    st = _lib.paged_attn_fwd_tree(
+        _dev(q, "q"), _dev(k_pages, "k_pages", q.dtype), _dev(v_pages, "v_pages", q.dtype),
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32),
+        _dev(query_lens, "query_lens", torch.int32), _dev(tree_mask, "tree_mask"),
+        _dev(out, "out", q.dtype), _dev(lse, "lse", torch.float32), ctypes.byref(dims),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check("paged_attn_fwd_tree", st)
 
 
 def spec_verify(p, q, draft_tokens, seed: int, accepted_len, out_tokens, *, stream=None) -> None:

@@ -83,6 +83,14 @@ constexpr int kNarrowRows = 16;    // units with at most this many rows take the
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
 constexpr int kUnitsPerSm = 16;    // split target: work units per SM
+// Row blocks in which some row sees fewer KV positions than this are "precise": with
+// few tokens each softmax weight is large, and one bf16 rounding of P (relative 2^-8)
+// would show in the output at the 1e-2 level.  The plan marks their items with
+// kItemPrecise in Item::split_rb; they run on the tcgen05 row-block path (whatever their
+// row count) with P in two bf16 parts, hi + lo, about 16 bits.  Such row blocks span at
+// most 64 + 128 positions (7 stages), so the extra product is cheap.
+constexpr int kPreciseTokens = 64;
+constexpr int32_t kItemPrecise = 1 << 30;
 constexpr int kPlanThreads = 256;
 constexpr int kPlanSmemSeqs = 4096;
 constexpr int kSeqInvalid = 1;
@@ -99,7 +107,7 @@ struct SeqPlan {
 };
 
 struct Item {
-  int32_t seq, page_begin, page_end, split_rb;  // split << kRbBits | row block
+  int32_t seq, page_begin, page_end, split_rb;  // split << kRbBits | row block (| kItemPrecise)
 };
 
 struct PlanHeader {
@@ -138,6 +146,7 @@ struct PlanArgs {
   void* out;
   float* lse;
   int32_t B, T, G, Hkv, Hq, D, P, maxp, pps, min_chunk, no_split, target_units, is_bf16;
+  const uint64_t* tree_mask;  // draft-tree masks, or null
   int64_t items_cap, partial_cap;
   int32_t* err;
 };
@@ -163,89 +172,96 @@ __device__ __forceinline__ int32_t splits_for(const SeqShape& s, int64_t chunk) 
   return (int32_t)((s.npages + chunk - 1) / chunk);
 }
 
-// Block-wide sums of three counters at once.
-__device__ __forceinline__ void block_sum3(int64_t& x, int64_t& y, int64_t& z, int64_t (*red)[3]) {
+// Block-wide sums of N counters at once.
+template <int N>
+__device__ __forceinline__ void block_sum(int64_t (&v)[N], int64_t (*red)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    x += __shfl_xor_sync(0xffffffffu, x, o);
-    y += __shfl_xor_sync(0xffffffffu, y, o);
-    z += __shfl_xor_sync(0xffffffffu, z, o);
-  }
+  for (int o = 16; o; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], o);
   __syncthreads();
-  if (lane == 0) {
-    red[warp][0] = x;
-    red[warp][1] = y;
-    red[warp][2] = z;
-  }
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < N; ++k) red[warp][k] = v[k];
   __syncthreads();
   const int nw = (int)(blockDim.x >> 5);
   if (warp == 0) {  // one warp combines the per-warp partials, the block reads the result
-    int64_t px = lane < nw ? red[lane][0] : 0, py = lane < nw ? red[lane][1] : 0,
-            pz = lane < nw ? red[lane][2] : 0;
+    int64_t pv[N];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      px += __shfl_xor_sync(0xffffffffu, px, o);
-      py += __shfl_xor_sync(0xffffffffu, py, o);
-      pz += __shfl_xor_sync(0xffffffffu, pz, o);
-    }
-    if (lane == 0) {
-      red[32][0] = px;
-      red[32][1] = py;
-      red[32][2] = pz;
-    }
+    for (int k = 0; k < N; ++k) pv[k] = lane < nw ? red[lane][k] : 0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < N; ++k) pv[k] += __shfl_xor_sync(0xffffffffu, pv[k], o);
+    if (lane == 0)
+#pragma unroll
+      for (int k = 0; k < N; ++k) red[32][k] = pv[k];
   }
   __syncthreads();
-  x = red[32][0];
-  y = red[32][1];
-  z = red[32][2];
+#pragma unroll
+  for (int k = 0; k < N; ++k) v[k] = red[32][k];
 }
 
-// Exclusive scans of three counters at once (threads in order); totals returned in t*.
-__device__ __forceinline__ void block_scan3(int64_t& x, int64_t& y, int64_t& z, int64_t (*red)[3],
-                                            int64_t& tx, int64_t& ty, int64_t& tz) {
+// Exclusive scans of N counters at once (threads in order); totals returned in t.
+template <int N>
+__device__ __forceinline__ void block_scan(int64_t (&v)[N], int64_t (*red)[4], int64_t (&t)[N]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t ix = x, iy = y, iz = z;
+  int64_t inc[N];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t nx = __shfl_up_sync(0xffffffffu, ix, o);
-    const int64_t ny = __shfl_up_sync(0xffffffffu, iy, o);
-    const int64_t nz = __shfl_up_sync(0xffffffffu, iz, o);
-    if (lane >= o) {
-      ix += nx;
-      iy += ny;
-      iz += nz;
+  for (int k = 0; k < N; ++k) inc[k] = v[k];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int64_t n = __shfl_up_sync(0xffffffffu, inc[k], o);
+      if (lane >= o) inc[k] += n;
     }
-  }
   __syncthreads();
-  if (lane == 31) {
-    red[warp][0] = ix;
-    red[warp][1] = iy;
-    red[warp][2] = iz;
-  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < N; ++k) red[warp][k] = inc[k];
   __syncthreads();
-  int64_t bx = 0, by = 0, bz = 0;
-  tx = ty = tz = 0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-    if (w < warp) {
-      bx += red[w][0];
-      by += red[w][1];
-      bz += red[w][2];
+  int64_t base[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) base[k] = t[k] = 0;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      if (w < warp) base[k] += red[w][k];
+      t[k] += red[w][k];
     }
-    tx += red[w][0];
-    ty += red[w][1];
-    tz += red[w][2];
-  }
-  x = bx + ix - x;
-  y = by + iy - y;
-  z = bz + iz - z;
+#pragma unroll
+  for (int k = 0; k < N; ++k) v[k] = base[k] + inc[k] - v[k];
+  __syncthreads();
 }
+
+// Whether row block rb of a sequence (query rows from qrow0) is precise: some row of it
+// sees fewer than kPreciseTokens positions.  A row of token j sees the context and, in
+// the causal window, tokens 0..j; in a draft tree its ancestors (mask bits below j) and
+// itself.  So a chain tree is classified exactly as the causal window.
+__device__ __forceinline__ bool rb_precise(const PlanArgs& a, const SeqShape& s, int64_t qrow0,
+                                           int rb) {
+  const int ctx = s.L - s.ql;
+  const int RB = row_block(s.R);
+  const int j0 = rb * RB / a.G;
+  if (a.tree_mask && s.ql > 1 && s.ql <= 64) {
+    const int j1 = min((rb + 1) * RB, s.R) - 1;
+    for (int j = j0; j <= j1 / a.G; ++j) {
+      const uint64_t below = j ? a.tree_mask[qrow0 + j] & (~0ull >> (64 - j)) : 0ull;
+      if (ctx + __popcll(below) + 1 < kPreciseTokens) return true;
+    }
+    return false;
+  }
+  return ctx + j0 + 1 < kPreciseTokens;
+}
+
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   pdl_wait_prior_grid();    // the previous kernel in the stream has released the workspace
   pdl_launch_dependents();  // the attention grid may start its prologue
   __shared__ int32_t s_L[kPlanSmemSeqs], s_ql[kPlanSmemSeqs];
-  __shared__ int64_t red[33][3];  // per-warp partials + the combined value
+  __shared__ int64_t red[33][4];  // per-warp partials + the combined value
   const int tid = threadIdx.x;
   const bool cached = a.B <= kPlanSmemSeqs;
   if (cached)
@@ -259,14 +275,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   };
 
   // Totals: work in page-row-blocks per KV head, packed query rows, invalid sequences.
-  int64_t cost = 0, rows = 0, bad = 0;
+  int64_t tot[3] = {0, 0, 0};  // cost, rows, bad
   for (int i = tid; i < a.B; i += kPlanThreads) {
     const SeqShape s = shape(i);
-    bad += !s.valid;
-    cost += (int64_t)s.npages * s.nrb;
-    rows += s.ql > 0 ? s.ql : 0;
+    tot[2] += !s.valid;
+    tot[0] += (int64_t)s.npages * s.nrb;
+    tot[1] += s.ql > 0 ? s.ql : 0;
   }
-  block_sum3(cost, rows, bad, red);
+  block_sum<3>(tot, red);
+  const int64_t cost = tot[0], rows = tot[1], bad = tot[2];
   const bool lengths_ok = rows == a.T && bad == 0;
   if (tid == 0 && !lengths_ok) atomicOr(a.err, VAS_DEV_BAD_LENGTHS);
 
@@ -281,23 +298,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     c = (c + a.pps - 1) / a.pps * a.pps;
   }
   for (int iter = 0; iter < 40; ++iter) {
-    int64_t n_items = 0, n_part = 0, unused = 0;
+    int64_t v[2] = {0, 0};  // items, partial rows
     for (int i = tid; i < a.B; i += kPlanThreads) {
       const SeqShape s = shape(i);
       const int32_t ns = splits_for(s, c);
-      n_items += (int64_t)ns * s.nrb;
-      if (ns > 1) n_part += (int64_t)ns * a.Hkv * s.R;
+      v[0] += (int64_t)ns * s.nrb;
+      if (ns > 1) v[1] += (int64_t)ns * a.Hkv * s.R;
     }
-    block_sum3(n_items, n_part, unused, red);
-    if ((n_items <= a.items_cap && n_part <= a.partial_cap) || c >= INT_MAX / 2) break;
+    block_sum<2>(v, red);
+    if ((v[0] <= a.items_cap && v[1] <= a.partial_cap) || c >= INT_MAX / 2) break;
     c = c * 2 < INT_MAX ? c * 2 : INT_MAX;
   }
   if (!lengths_ok)  // the row -> sequence map is only needed to find rows to NaN-fill
     for (int r = tid; r < a.T; r += kPlanThreads) a.token_seq[r] = -1;
   __syncthreads();
 
-  // Scans in batch order, kPlanThreads sequences at a time.
-  int64_t carry_rows = 0, carry_items = 0, carry_part = 0;
+  // Scans in batch order, kPlanThreads sequences at a time.  A sequence's items are
+  // (split, row block) pairs, split-major, from item0 on; its merge counters sit there
+  // too.
+  int64_t carry[3] = {0, 0, 0};  // rows, items, partial rows
   for (int base = 0; base < a.B; base += kPlanThreads) {
     const int i = base + tid;
     SeqShape s;
@@ -309,13 +328,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       qrows = s.ql > 0 ? s.ql : 0;
       ns = splits_for(s, c);
     }
-    int64_t my_row0 = qrows, my_item0 = (int64_t)ns * s.nrb;
-    int64_t my_part0 = ns > 1 ? (int64_t)ns * a.Hkv * s.R : 0;
-    int64_t t_rows, t_items, t_part;
-    block_scan3(my_row0, my_item0, my_part0, red, t_rows, t_items, t_part);
-    my_row0 += carry_rows;
-    my_item0 += carry_items;
-    my_part0 += carry_part;
+    int64_t v[3] = {qrows, (int64_t)ns * s.nrb, ns > 1 ? (int64_t)ns * a.Hkv * s.R : 0};
+    int64_t t[3];
+    block_scan<3>(v, red, t);
+    const int64_t my_row0 = v[0] + carry[0];
+    const int64_t my_item0 = v[1] + carry[1];
+    const int64_t my_part0 = v[2] + carry[2];
     if (i < a.B) {
       SeqPlan sp;
       sp.qrow0 = (int32_t)my_row0;
@@ -336,17 +354,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       if (!lengths_ok)
         for (int j = 0; j < qrows && my_row0 + j < a.T; ++j) a.token_seq[my_row0 + j] = i;
       if (ns > 0) {
-        // A skipped sequence keeps its slots below the capacity as null items.
+        // A skipped sequence keeps its slots below the capacity as null items.  The
+        // tree masks of a skipped sequence's rows may not exist (rows past T).
         int64_t it = my_item0;
         for (int sp_i = 0; sp_i < ns; ++sp_i) {
           const int32_t pb = (int32_t)(sp_i * c);
           const int32_t pe = (int32_t)((sp_i + 1) * c < s.npages ? (sp_i + 1) * c : s.npages);
           for (int rb = 0; rb < s.nrb && it < a.items_cap; ++rb) {
+            const bool prec = a.is_bf16 && sp.nsplit > 0 && rb_precise(a, s, my_row0, rb);
             Item item;
             item.seq = sp.nsplit > 0 ? i : -1;
             item.page_begin = pb;
             item.page_end = pe;
-            item.split_rb = (sp_i << kRbBits) | rb;
+            item.split_rb = (sp_i << kRbBits) | rb | (prec ? kItemPrecise : 0);
             a.items[it++] = item;
           }
         }
@@ -354,15 +374,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
       if (sp.nsplit > 1)  // arrival counters of the last-split merge
         for (int k = 0; k < s.nrb * a.Hkv; ++k) a.counters[(size_t)sp.item0 * a.Hkv + k] = 0;
     }
-    carry_rows += t_rows;
-    carry_items += t_items;
-    carry_part += t_part;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) carry[k] += t[k];
   }
   if (tid == 0) {
-    a.header->n_items = (int32_t)(carry_items < a.items_cap ? carry_items : a.items_cap);
+    a.header->n_items = (int32_t)(carry[1] < a.items_cap ? carry[1] : a.items_cap);
     a.header->work_counter = 0;
     a.header->chunk_pages = (int32_t)(c < INT_MAX ? c : INT_MAX);
-    a.header->n_partial_rows = (int32_t)carry_part;
+    a.header->n_partial_rows = (int32_t)carry[2];
   }
   if (lengths_ok) return;
   __syncthreads();
@@ -405,6 +424,7 @@ struct AttnArgs {
   float scale_log2;  // softmax scale * log2(e)
   float scale;
   int32_t* err;
+  const uint64_t* tree_mask;  // draft-tree visibility per query token, or null (causal)
 };
 
 template <int D>
@@ -427,7 +447,9 @@ struct Smem {
   // Prompt-chunk units: their query tile (128 rows, K-major 128-byte swizzle,
   // [D/64][row][64]) after the P tiles.
   static constexpr int kQTileOff = kPTileOff + 2 * kPTileBytes;
-  static constexpr int kWideBytes = kQTileOff + 128 * D * 2;
+  // Precise units: the rounding error of each P tile as a second bf16 tile.
+  static constexpr int kPLoOff = kQTileOff + 128 * D * 2;
+  static constexpr int kWideBytes = kPLoOff + 2 * kPTileBytes;
   static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
@@ -437,8 +459,12 @@ struct Smem {
   // barriers bp[2], bo[2], bs[2], bq, bfin | meta[kSlots], flag[4], tmem base
   static constexpr int kWideBars = 8;
   static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars) * 8 + (kSlots + 4 + 1) * 4;
-  static constexpr int kBytes = kBarOff + kBarBytes;
+  // Draft-tree masks of the unit's rows (row r: its token's mask, own bit set).
+  static constexpr int kTmaskOff = ((kBarOff + kBarBytes + 7) / 8) * 8;
+  static constexpr int kBytes = kTmaskOff + kRowBlockTc * 8;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kDynBytes <= 227 * 1024, "shared memory of one CTA");
+  static_assert(kPLoOff % 1024 == 0 && kQTileOff % 1024 == 0, "swizzle atoms of the tiles");
 };
 
 // Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage.
@@ -465,14 +491,18 @@ __host__ __device__ constexpr uint32_t tok_off(int t) {
 constexpr float kRebase = 8.f;
 
 // Per-lane ldmatrix byte offsets (relative to a stage operand) for the narrow path:
-// koff[ks]: K A-fragment of token tile 0, k-step ks; voff[dt]: V^T A-fragment of token
-// tile 0, d-tile dt.  Token tile 1 adds 16 rows.
+// koff[ks % 4]: K A-fragment of token tile 0, k-step ks; voff[dt % 4]: V^T A-fragment of
+// token tile 0, d-tile dt.  Steps 4 apart are the same chunks of the next 64-column
+// half (half_off), and token tile 1 adds 16 rows: both are immediates.
+template <int P>
+__host__ __device__ constexpr uint32_t half_off(int i) {
+  return (uint32_t)(i >> 2) * (P * 128);
+}
 template <int D, int P>
-__device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[D / 16],
-                                               uint32_t (&voff)[D / 16]) {
+__device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[4], uint32_t (&voff)[4]) {
   const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
-  for (int i = 0; i < D / 16; ++i) {
+  for (int i = 0; i < 4; ++i) {
     koff[i] = kv_off<D, P>((mi & 1) * 8 + r8, 2 * i + (mi >> 1));
     voff[i] = kv_off<D, P>((mi >> 1) * 8 + r8, 2 * i + (mi & 1));
   }
@@ -482,11 +512,12 @@ __device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[D / 16
 template <int D, int P, int NN, bool MASKED>
 __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int loaded,
                                              const uint32_t (&qb)[D / 16][NN][2],
-                                             const uint32_t (&koff)[D / 16],
-                                             const uint32_t (&voff)[D / 16],
+                                             const uint32_t (&koff)[4],
+                                             const uint32_t (&voff)[4],
                                              float (&oT)[D / 16][NN][4], float (&mref)[NN][2],
                                              float (&l)[NN][2], int t_abs0,
-                                             const int (&lim)[NN][2], float c, int lane) {
+                                             const int (&lim)[NN][2], float c, int lane,
+                                             const uint64_t* tm, int ctx_end) {
   constexpr uint32_t kTile = tok_off<D, P>(16);  // 16 token rows
   const int g = lane >> 2;
   float s[2][NN][4];
@@ -501,7 +532,7 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4(kbase + koff[ks] + mt * kTile, a[0], a[1], a[2], a[3]);
+        ldsm_x4(kbase + koff[ks & 3] + half_off<P>(ks) + mt * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(acc[ks & 1][nn], a, qb[ks][nn][0], qb[ks][nn][1]);
       }
@@ -521,6 +552,23 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
           const int tt = 16 * mt + g + 8 * (e >> 1);
           if (tt >= loaded || t_abs0 + tt > lim[nn][e & 1]) s[mt][nn][e] = -INFINITY;
         }
+    // Draft tree: in the draft window (positions from ctx_end on) a row keeps only its
+    // ancestors and itself.  Scores already past the causal limit stay dropped.
+    if (tm != nullptr) {
+#pragma unroll
+      for (int nn = 0; nn < NN; ++nn)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t mk = tm[8 * nn + 2 * (lane & 3) + h];
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+              const int dt = t_abs0 + 16 * mt + g + 8 * hi - ctx_end;
+              if (dt >= 0 && !((mk >> (dt & 63)) & 1)) s[mt][nn][2 * hi + h] = -INFINITY;
+            }
+        }
+    }
   }
 
   // Rebase the rows whose maximum outgrew the reference.
@@ -586,7 +634,7 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
         uint32_t a[4];
-        ldsm_x4_trans(vbase + voff[dt] + kk * kTile, a[0], a[1], a[2], a[3]);
+        ldsm_x4_trans(vbase + voff[dt & 3] + half_off<P>(dt) + kk * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
       }
@@ -595,12 +643,12 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
 }
 
 // Per-lane ldmatrix byte offsets of the K B-fragments of the wide path: token tile 0
-// (8 rows), d-chunks 4 qd .. 4 qd + 3.
+// (8 rows), d-chunks 4 qd .. 4 qd + 3 at kw[qd % 2] + half_off(2 qd).
 template <int D, int P>
-__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32]) {
+__device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[2]) {
   const int mi = lane >> 3, r8 = lane & 7;
 #pragma unroll
-  for (int i = 0; i < D / 32; ++i) kw[i] = kv_off<D, P>(r8, 4 * i + mi);
+  for (int i = 0; i < 2; ++i) kw[i] = kv_off<D, P>(r8, 4 * i + mi);
 }
 
 // ---- wide units: S = Q K^T of one m16 row tile over a step, in registers -------------
@@ -613,10 +661,10 @@ __device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[D / 32]) {
 template <int D, int P, int NST>
 __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid, bool masked,
                                             const uint32_t (&qa)[D / 16][4],
-                                            const uint32_t (&kw)[D / 32], float (&mref)[2],
+                                            const uint32_t (&kw)[2], float (&mref)[2],
                                             float (&l)[2], float (&alpha)[2], bool& rescale,
                                             int t_abs0, int limA, int limB, float c, int lane,
-                                            uint8_t* prow) {
+                                            uint8_t* prow, const uint64_t* tmw, int ctx_end) {
   constexpr int NT = 4 * NST;
   const int g = lane >> 2, tq = lane & 3;
   float s[NT][4];
@@ -630,17 +678,23 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb[nt >> 2] + kw[qd] + tok_off<D, P>(8 * (nt & 3)), b0, b1, b2, b3);
+      ldsm_x4(kb[nt >> 2] + kw[qd & 1] + half_off<P>(2 * qd) + tok_off<D, P>(8 * (nt & 3)), b0,
+              b1, b2, b3);
       mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
       mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
     }
   if (masked) {
+    // Draft tree: rows g and g + 8 keep only their ancestors (and themselves) among the
+    // draft tokens (positions from ctx_end on).
+    const uint64_t mA = tmw ? tmw[0] : ~0ull, mB = tmw ? tmw[8] : ~0ull;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tt = 8 * nt + 2 * tq + (e & 1);
-        if (tt >= tvalid || t_abs0 + tt > ((e < 2) ? limA : limB)) s[nt][e] = -INFINITY;
+        const int dt = t_abs0 + tt - ctx_end;
+        const bool in_tree = dt < 0 || (((e < 2) ? mA : mB) >> (dt & 63)) & 1;
+        if (tt >= tvalid || t_abs0 + tt > ((e < 2) ? limA : limB) || !in_tree) s[nt][e] = -INFINITY;
       }
   }
   float mx[2] = {-INFINITY, -INFINITY};
@@ -680,6 +734,53 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
     *reinterpret_cast<uint32_t*>(prow + off) = pack_bf16x2(p[0], p[1]);
     *reinterpret_cast<uint32_t*>(prow + 8 * 128 + off) = pack_bf16x2(p[2], p[3]);
   }
+}
+
+// ---- prompt-chunk units: one row of P ---------------------------------------------------
+// Row r's 32 scores sr (fp32 bits, raw Q K^T) of one stage to probabilities against the
+// reference maximum mu (scaled by c), written as bf16 into its 128-byte row of the P
+// tile (K-major, 128-byte swizzle); tokens outside `valid` get 0.  Returns the row's sum
+// of P.  A precise unit also writes each value's bf16 rounding error into the low tile
+// (O += P_lo V follows O += P V).
+template <int D, bool PRECISE>
+__device__ __forceinline__ float chunk_p_row(const uint32_t (&sr)[32], uint32_t valid, float c,
+                                             float mu, uint8_t* prow, int r) {
+  float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t hw[16];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float e0 = ex2_approx(fmaf(__uint_as_float(sr[i]), c, -mu));
+    const float e1 = ex2_approx(fmaf(__uint_as_float(sr[i + 1]), c, -mu));
+    const float p0 = (valid >> i) & 1 ? e0 : 0.f;
+    const float p1 = (valid >> (i + 1)) & 1 ? e1 : 0.f;
+    const uint32_t h = pack_bf16x2(p0, p1);
+    hw[i >> 1] = h;
+    s4[(i >> 1) & 3] += p0 + p1;
+    if constexpr (PRECISE) {
+      // The low part goes out at once: its 16 words are never live together.
+      const uint32_t lo = pack_bf16x2(p0 - bf16_lo_f32(h), p1 - bf16_hi_f32(h));
+      *reinterpret_cast<uint32_t*>(prow + (Smem<D>::kPLoOff - Smem<D>::kPTileOff) +
+                                   (((i >> 3) ^ (r & 7)) << 4) + (i & 7) * 2) = lo;
+    }
+  }
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch)
+    *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
+        make_uint4(hw[4 * ch], hw[4 * ch + 1], hw[4 * ch + 2], hw[4 * ch + 3]);
+  return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
+// ---- unit classification ------------------------------------------------------------
+// Draft-tree units: sequences with 2..64 query tokens when a tree is given; longer
+// query windows (prompt chunks) and decode rows keep the causal window.
+__device__ __forceinline__ bool tree_unit(const AttnArgs& a, int ql) {
+  return a.tree_mask != nullptr && ql > 1 && ql <= 64;
+}
+// The smallest position limit over the rows of a row block starting at row r0: the
+// causal limit of its first token, or for a tree the last context position (any draft
+// token may be hidden from a row).
+__device__ __forceinline__ int unit_min_lim(const AttnArgs& a, int L, int ql, int r0) {
+  return tree_unit(a, ql) ? L - ql - 1 : L - ql + r0 / a.G;
 }
 
 // ---- output helpers ----------------------------------------------------------------
@@ -844,6 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait_prior_grid();  // the plan of this call is complete and visible
 
   const int32_t n_units = a.header->n_items * a.Hkv;
+  int32_t* const work_counter = &a.header->work_counter;
 
   if (warp == kProducerWarp) {
     // ------------------------------ producer ------------------------------
@@ -854,8 +956,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first block-table chunk are in flight, and the atomic for the one after.
     int32_t u = 0, u1 = 0, u2_lane0 = 0;
     if (lane == 0) {
-      u = atomicAdd(&a.header->work_counter, 1);
-      u1 = atomicAdd(&a.header->work_counter, 1);
+      u = atomicAdd(work_counter, 1);
+      u1 = atomicAdd(work_counter, 1);
     }
     u = __shfl_sync(0xffffffffu, u, 0);
     u1 = __shfl_sync(0xffffffffu, u1, 0);
@@ -869,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       it1 = a.items[u1 / a.Hkv];
       if (it1.seq >= 0) sp1 = a.seqplan[it1.seq];
     }
-    if (lane == 0) u2_lane0 = atomicAdd(&a.header->work_counter, 1);
+    if (lane == 0) u2_lane0 = atomicAdd(work_counter, 1);
     int32_t bt_cur = 0;  // this lane's block-table entry of the unit's first 32 pages
     if (u < n_units && it.seq >= 0 && it.page_begin + lane < it.page_end)
       bt_cur = a.block_table[(size_t)it.seq * a.maxp + it.page_begin + lane];
@@ -903,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Item it2{};
       SeqPlan sp2{};
       if (u2 < n_units) it2 = a.items[u2 / a.Hkv];
-      if (lane == 0) u2_lane0 = atomicAdd(&a.header->work_counter, 1);
+      if (lane == 0) u2_lane0 = atomicAdd(work_counter, 1);
 
       if (it.seq >= 0) {
         const int head = u % a.Hkv;
@@ -984,6 +1086,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kDescHi = umma_desc_hi_sw128(1024);
     const uint32_t p_lo = umma_desc_lo(smem_u32(scratch + S::kPTileOff), 16);  // P tile 0
     const uint32_t q_lo = umma_desc_lo(smem_u32(scratch + S::kQTileOff), 16);
+    constexpr uint32_t kPLoDesc = (S::kPLoOff - S::kPTileOff) >> 4;  // descriptor units
     for (;;) {
       const int slot = unit_it % kRing;
       if (!mbar_wait(&ufull[slot], (unit_it / kRing) & 1)) {
@@ -1000,12 +1103,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
       const int R = a.G * re.sp.qlen;
       const int RB = row_block(R);
-      const int Rb = min(RB, R - (it.split_rb & ((1 << kRbBits) - 1)) * RB);
-      if (n_stages == 0 || (RB == kRowBlock && Rb <= kNarrowRows)) {  // consumer warps alone
+      const int r0 = (it.split_rb & ((1 << kRbBits) - 1)) * RB;
+      const int Rb = min(RB, R - r0);
+      const bool precise = (it.split_rb & kItemPrecise) != 0;
+      if (n_stages == 0 || (!precise && RB == kRowBlock && Rb <= kNarrowRows)) {  // consumers alone
         stage_it += n_stages;
         continue;
       }
-      if (RB == kRowBlockTc) {
+      if (RB == kRowBlockTc || precise) {
         // A prompt-chunk unit, one step per stage.  S_k = Q K_k^T into S buffer k & 1
         // (M 128 lanes; N the stage's 32 tokens, as two 16-token products with 16-token
         // pages) once the query tile is staged and the stage has landed; O += P_k V_k
@@ -1039,31 +1144,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           return true;
         };
-        ok = issue_s(0) && (n_stages < 2 || issue_s(1));
-        for (int j = 0; ok && j < n_stages; ++j) {
-          const uint32_t k = wk + j, b = k & 1;
-          if (!mbar_wait(&bp[b], (k >> 1) & 1)) {
-            ok = false;
-            break;
+        // The stage loop comes in two copies: a precise unit adds O += P_lo V after each
+        // O += P V (this loop is the issue-bound part of prompt chunks, and a branch in
+        // it costs them).
+        auto stages_pv = [&](auto prec) {
+          bool good = issue_s(0) && (n_stages < 2 || issue_s(1));
+          for (int j = 0; good && j < n_stages; ++j) {
+            const uint32_t k = wk + j, b = k & 1;
+            if (!mbar_wait(&bp[b], (k >> 1) & 1)) {
+              good = false;
+              break;
+            }
+            if (lane == 0) {
+              tc_fence_after();
+              const uint32_t st = stage_it + j;
+              const int slot_s = st % kSlots;
+              const int pg = it.page_begin + j * PPS;
+              const int loaded = min(PPS, it.page_end - pg) * P;
+              const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
+              const uint32_t v_lo = umma_desc_lo(
+                  smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
+              for (int kk = 0; kk < loaded / 16; ++kk)
+                umma_bf16_lh(tmem + kTmemO, pb_lo + ((kk * 32) >> 4),
+                             v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO, j > 0 || kk > 0);
+              if constexpr (decltype(prec)::value)
+                for (int kk = 0; kk < loaded / 16; ++kk)
+                  umma_bf16_lh(tmem + kTmemO, pb_lo + kPLoDesc + ((kk * 32) >> 4),
+                               v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO, true);
+              umma_commit(&empty[slot_s]);
+              umma_commit(&bo[b]);
+            }
+            __syncwarp();
+            if (j + 2 < n_stages) good = issue_s(j + 2);
           }
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t st = stage_it + j;
-            const int slot_s = st % kSlots;
-            const int pg = it.page_begin + j * PPS;
-            const int loaded = min(PPS, it.page_end - pg) * P;
-            const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
-            const uint32_t v_lo = umma_desc_lo(
-                smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
-            for (int kk = 0; kk < loaded / 16; ++kk)
-              umma_bf16_lh(tmem + kTmemO, pb_lo + ((kk * 32) >> 4), v_lo + (tok_off<D, P>(16 * kk) >> 4),
-                           kDescHi, kIdO, j > 0 || kk > 0);
-            umma_commit(&empty[slot_s]);
-            umma_commit(&bo[b]);
-          }
-          __syncwarp();
-          if (j + 2 < n_stages) ok = issue_s(j + 2);
-        }
+          return good;
+        };
+        ok = precise ? stages_pv(std::true_type{}) : stages_pv(std::false_type{});
         wk += n_stages;
         wc += n_stages;
         stage_it += n_stages;
@@ -1150,7 +1266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (it.seq < 0) continue;
     const SeqPlan sp = re.sp;
     const int head = re.head;
-    const int split = it.split_rb >> kRbBits, rb = it.split_rb & ((1 << kRbBits) - 1);
+    const int split = (it.split_rb & ~kItemPrecise) >> kRbBits;
+    const int rb = it.split_rb & ((1 << kRbBits) - 1);
+    const bool precise = (it.split_rb & kItemPrecise) != 0;
     const int L = sp.len, ql = sp.qlen;
     const int R = a.G * ql;
     const int RB = row_block(R);
@@ -1158,9 +1276,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int Rb = min(RB, R - r0);
     const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
     const uint32_t stage0 = stage_it;  // first stage of this unit in the CTA's stream
-    const int min_lim = L - ql + r0 / a.G;  // smallest causal limit of this row block
+    // Draft tree (at most 64 query tokens; longer chunks keep the causal window): its
+    // rows' masks go to shared memory, own bit set, and no stage that reaches the draft
+    // window counts as interior.
+    const int ctx_end = L - ql;
+    const bool tree = tree_unit(a, ql);
+    uint64_t* tm = tree ? reinterpret_cast<uint64_t*>(smem + S::kTmaskOff) : nullptr;
+    if (tree) {
+      const int j = (r0 + tid) / a.G;
+      tm[tid] = tid < Rb ? a.tree_mask[sp.qrow0 + j] | (1ull << j) : ~0ull;
+    }
+    const int min_lim = unit_min_lim(a, L, ql, r0);
 
-    const bool chunk = RB == kRowBlockTc && n_stages > 0;  // prompt chunk: tcgen05 S and PV
+    // Prompt-chunk and precise row blocks: tcgen05 S and PV, rows in TMEM lanes.
+    const bool chunk = (RB == kRowBlockTc || precise) && n_stages > 0;
     const bool wide = !chunk && Rb > kNarrowRows && n_stages > 0;
     if (chunk) {
       // The query tile for tcgen05 S: rows 0 .. Rb-1 (row r: token r / G, head
@@ -1241,7 +1370,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + kTmemS + (kc & 1) * 32, sr);
           // Valid tokens of this row form a prefix of the stage: i < loaded, t <= lim.
           const int nv = row_ok ? max(0, min(loaded, lim - t_abs0 + 1)) : 0;
-          const uint32_t valid = nv >= 32 ? 0xffffffffu : (1u << nv) - 1u;
+          uint32_t valid = nv >= 32 ? 0xffffffffu : (1u << nv) - 1u;
+          // Draft tree: token i of the stage is draft token i - d0 when i >= d0.
+          const int d0 = ctx_end - t_abs0;
+          if (tree && d0 < 32) {
+            const uint64_t mr = tm[r];
+            valid &= d0 > 0 ? (uint32_t)(mr << d0) | ((1u << d0) - 1u)
+                            : (-d0 < 64 ? (uint32_t)(mr >> -d0) : 0u);
+          }
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int i = 0; i < 32; ++i)
@@ -1270,23 +1406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const float mu = mref == -INFINITY ? 0.f : mref;
-          uint32_t pw[16];
-          float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(sr[i]), c, -mu));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(sr[i + 1]), c, -mu));
-            const float p0 = (valid >> i) & 1 ? e0 : 0.f;
-            const float p1 = (valid >> (i + 1)) & 1 ? e1 : 0.f;
-            s4[(i >> 1) & 3] += p0 + p1;
-            pw[i >> 1] = pack_bf16x2(p0, p1);
-          }
-          l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
           uint8_t* prow = scratch + S::kPTileOff + b * S::kPTileBytes + r * 128;
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch)
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-                make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]);
+          l += precise ? chunk_p_row<D, true>(sr, valid, c, mu, prow, r)
+                       : chunk_p_row<D, false>(sr, valid, c, mu, prow, r);
           fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -1359,7 +1481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qb[2 * kp][nn][1], qb[2 * kp + 1][nn][0],
                     qb[2 * kp + 1][nn][1]);
           }
-        uint32_t koff[D / 16], voff[D / 16];
+        uint32_t koff[4], voff[4];
         narrow_offsets<D, P>(lane, koff, voff);
         float oT[D / 16][NN][4];
 #pragma unroll
@@ -1404,10 +1526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
             narrow_stage<D, P, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                       lim, a.scale_log2, lane);
+                                          lim, a.scale_log2, lane, tm, ctx_end);
           else
             narrow_stage<D, P, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                      lim, a.scale_log2, lane);
+                                         lim, a.scale_log2, lane, tm, ctx_end);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot_s]);
         }
@@ -1504,7 +1626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   qa[ks][2], qa[ks][3]);
         }
       }
-      uint32_t kw[D / 32];
+      uint32_t kw[2];
       wide_offsets<D, P>(lane, kw);
       named_bar_sync(1, kConsumerThreads);  // the query staging becomes the P tiles
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
@@ -1512,6 +1634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rA = r0 + 16 * warp + g, rB = rA + 8;
       const int limA = rA < R ? L - ql + rA / a.G : L - 1;
       const int limB = rB < R ? L - ql + rB / a.G : L - 1;
+      const uint64_t* tmw = tm ? tm + 16 * warp + g : nullptr;
       const int n_steps = (n_stages + 1) >> 1;
       for (int sj = 0; sj < n_steps; ++sj) {
         const uint32_t k = wk + sj, b = k & 1;
@@ -1562,10 +1685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool rescale;
           if (nst == 2)
             wide_s_step<D, P, 2>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
-                              limB, a.scale_log2, lane, prow);
+                              limB, a.scale_log2, lane, prow, tmw, ctx_end);
           else
             wide_s_step<D, P, 1>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
-                              limB, a.scale_log2, lane, prow);
+                              limB, a.scale_log2, lane, prow, tmw, ctx_end);
           if (__any_sync(0xffffffffu, rescale && sj > 0)) {
             // O holds the products up to the previous step: wait for the last of them,
             // then scale row 16 w + t (lane t < 16) by its factor (held by lane 4 (t % 8)).
@@ -1694,6 +1817,10 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
       const int j = r / a.G;
       const int pos = L - ql + j;
       const size_t orow = out_row(a, sp, head, r);
+      // Draft tree: among the draft tokens (positions from L - ql on) only the ancestors
+      // and the token itself are visible.
+      const bool tree = tree_unit(a, ql);
+      const uint64_t vis = tree ? a.tree_mask[sp.qrow0 + j] | (1ull << j) : ~0ull;
       __syncwarp();
 #pragma unroll
       for (int e = 0; e < E; ++e) qs[warp][lane + 32 * e] = qg[orow * D + lane + 32 * e];
@@ -1712,6 +1839,8 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
           if (page < 0 || page >= a.num_pages) {
             bad = true;
             page = -1;
+          } else if (t >= L - ql && !((vis >> ((t - (L - ql)) & 63)) & 1)) {
+            page = -1;  // outside the tree: no score, no value row
           } else {
             const float* krow = kp + (((size_t)page * a.P + t % a.P) * a.Hkv + head) * D;
             float dot = 0.f;
@@ -1905,11 +2034,14 @@ size_t paged_attn_workspace_size(const vas_attn_dims* dims) {
       .total;
 }
 
-int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
-                   const int32_t* block_table, const int32_t* seq_lens,
-                   const int32_t* query_lens, void* out, float* lse,
-                   const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
-                   vas_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+int attn_launch(const void* q, const void* k_pages, const void* v_pages,
+                const int32_t* block_table, const int32_t* seq_lens, const int32_t* query_lens,
+                const uint64_t* tree_mask, void* out, float* lse, const vas_attn_dims* dims,
+                void* workspace, size_t workspace_bytes, vas_stream_t stream_) {
   if (!dims_ok(dims)) return VAS_E_INVALID_ARG;
   if (!dims_supported(dims)) return VAS_E_UNSUPPORTED;
   const vas_attn_dims& d = *dims;
@@ -1919,7 +2051,8 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
     return VAS_E_INVALID_ARG;
   auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
   if (mis(q, 16) || mis(k_pages, 16) || mis(v_pages, 16) || mis(out, 16) || mis(lse, 4) ||
-      mis(block_table, 4) || mis(seq_lens, 4) || mis(query_lens, 4) || mis(workspace, 256))
+      mis(block_table, 4) || mis(seq_lens, 4) || mis(query_lens, 4) || mis(workspace, 256) ||
+      mis(tree_mask, 8))
     return VAS_E_INVALID_ARG;
   if (d.num_pages == 0 || d.max_pages_per_seq == 0) return VAS_E_INVALID_ARG;
   if ((int64_t)d.num_pages * d.page_size > INT32_MAX) return VAS_E_INVALID_ARG;
@@ -1959,6 +2092,7 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   pa.no_split = bf16 ? 0 : 1;
   pa.target_units = kUnitsPerSm * sms;
   pa.is_bf16 = bf16 ? 1 : 0;
+  pa.tree_mask = tree_mask;
   pa.items_cap = lay.items_cap;
   pa.partial_cap = lay.partial_cap;
   pa.err = err;
@@ -2002,6 +2136,7 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   aa.scale = scale;
   aa.scale_log2 = scale * 1.4426950408889634f;
   aa.err = err;
+  aa.tree_mask = tree_mask;
 
   if (bf16) {
     CUtensorMap mk, mv;
@@ -2017,6 +2152,29 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
   if (d.head_dim == 128) attn_f32_kernel<128><<<grid, 128, 0, stream>>>(aa);
   else attn_f32_kernel<64><<<grid, 128, 0, stream>>>(aa);
   return cudaGetLastError() == cudaSuccess ? VAS_OK : VAS_E_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
+                   const int32_t* block_table, const int32_t* seq_lens,
+                   const int32_t* query_lens, void* out, float* lse,
+                   const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
+                   vas_stream_t stream) {
+  return attn_launch(q, k_pages, v_pages, block_table, seq_lens, query_lens, nullptr, out, lse,
+                     dims, workspace, workspace_bytes, stream);
+}
+
+int paged_attn_fwd_tree(const void* q, const void* k_pages, const void* v_pages,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        const int32_t* query_lens, const uint64_t* tree_mask, void* out,
+                        float* lse, const vas_attn_dims* dims, void* workspace,
+                        size_t workspace_bytes, vas_stream_t stream) {
+  if (!tree_mask) return VAS_E_INVALID_ARG;
+  return attn_launch(q, k_pages, v_pages, block_table, seq_lens, query_lens, tree_mask, out, lse,
+                     dims, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

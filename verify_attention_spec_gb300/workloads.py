@@ -211,6 +211,22 @@ def attention_inputs(lens, qlens, *, num_q_heads, num_kv_heads, head_dim, page_s
                            num_kv_heads, head_dim, page_size, kv_dtype)
 
 
+def draft_tree_parents(qlens, seed: int, extra_roots: float = 0.0) -> np.ndarray:
+    """A random draft tree per sequence: int32 [sum(qlens)], each query token's parent as
+    an index among its own sequence's query tokens, -1 for a root.  Token 0 is the root
+    (the last accepted token); token j > 0 hangs under a uniformly drawn earlier token (a
+    random recursive tree: bushy near the root, as top-k drafting makes it), or becomes a
+    root of its own with probability `extra_roots` (a forest)."""
+    rng = _rng(seed, 3)
+    out = []
+    for ql in np.asarray(qlens, dtype=np.int64):
+        par = np.full(int(ql), -1, dtype=np.int32)
+        for j in range(1, int(ql)):
+            par[j] = -1 if rng.random() < extra_roots else int(rng.integers(0, j))
+        out.append(par)
+    return np.concatenate(out) if out else np.zeros(0, dtype=np.int32)
+
+
 def workload_attention(name: str, pool_device="cpu") -> AttentionInputs:
     w = WORKLOADS[name]
     return attention_inputs(sample_lengths(w), query_lengths(w), num_q_heads=w.num_q_heads,
