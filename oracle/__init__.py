@@ -25,6 +25,7 @@ _lock = threading.Lock()
 _lib = None
 
 F32, BF16, F64 = 0, 1, 2
+Q_E4M3, Q_INT8 = 0, 1  # quantised KV formats (oracle.c: oracle_dequant_kv)
 OK, E_ARG, E_PAGE, E_LEN, E_TOKEN, E_DIST = 0, -1, -2, -3, -4, -5
 
 # Decisions whose uniform lies within this distance of its threshold are flagged
@@ -59,6 +60,8 @@ def _load():
     lib.oracle_paged_attn_tree.argtypes = [P, P, P, i32, P, P, P, P, i32, i32, i32, i32, i32,
                                            i32, i32, dbl, P, P]
     lib.oracle_paged_attn_tree.restype = i32
+    lib.oracle_dequant_kv.argtypes = [P, P, i32, i64, i32, i32, i32, P]
+    lib.oracle_dequant_kv.restype = i32
     lib.oracle_philox4x32_10.argtypes = [P, P, P]
     lib.oracle_philox4x32_10.restype = None
     lib.oracle_philox4x32_10_many.argtypes = [P, i64, P, P]
@@ -132,6 +135,32 @@ def paged_attn(q, k_pages, v_pages, block_table, seq_lens, query_lens, *, dtype_
     if rc != OK:
         raise ValueError(f"oracle_paged_attn rejected its arguments (code {rc})")
     return out, lse
+
+
+def dequant_kv(codes, scales, fmt: int) -> np.ndarray:
+    """Decode a quantised page pool (oracle.c: oracle_dequant_kv).  codes uint8
+    [num_pages, P, Hkv, D]; scales float32 [num_pages, Hkv, P].  Returns float64
+    [num_pages, P, Hkv, D]."""
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    n, P, Hkv, D = c.shape
+    assert sc.shape == (n, Hkv, P)
+    out = np.empty(c.shape, dtype=np.float64)
+    rc = lib.oracle_dequant_kv(_ptr(c), _ptr(sc), int(fmt), n, P, Hkv, D, _ptr(out))
+    if rc != OK:
+        raise ValueError(f"oracle_dequant_kv rejected its arguments (code {rc})")
+    return out
+
+
+def paged_attn_quant(q_bf16_bits, k_codes, v_codes, k_scale, v_scale, block_table, seq_lens,
+                     query_lens, *, fmt: int, scale: float | None = None, parents=None):
+    """Attention over a quantised pool: the pool decoded exactly (dequant_kv), then the
+    float64 attention of paged_attn.  q is given as raw bf16 bits [T, Hq, D]."""
+    qf = (np.ascontiguousarray(q_bf16_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return paged_attn(qf.astype(np.float64), dequant_kv(k_codes, k_scale, fmt),
+                      dequant_kv(v_codes, v_scale, fmt), block_table, seq_lens, query_lens,
+                      dtype_code=F64, scale=scale, parents=parents)
 
 
 def philox4x32_10(counters: np.ndarray, key) -> np.ndarray:

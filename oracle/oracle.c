@@ -229,6 +229,52 @@ int oracle_paged_attn_tree(const void* q, const void* k_pages, const void* v_pag
 }
 
 /* ------------------------------------------------------------------------------
+ * Quantised KV pages ("llm-inference-optimization-batching", tempatgunting.com,
+ * section "Quantization and Precision Choices for KV": INT8 or FP8 KV with per-head
+ * or per-token scaling factors, separate scales for K and V, dequantised inside the
+ * attention).  Reading: one scale per (page, KV head, slot), i.e. per token and head,
+ * symmetric (no zero point); value = scale * decode(code).
+ *
+ * codes  [num_pages, page_size, num_kv_heads, head_dim] bytes (the pool layout);
+ * scales [num_pages, num_kv_heads, page_size] fp32;
+ * out    [num_pages, page_size, num_kv_heads, head_dim] double.
+ * fmt ORC_Q_E4M3: OCP FP8 E4M3 ("fn": no infinities) -- sign bit, 4 exponent bits with
+ *   bias 7, 3 mantissa bits; exponent 0 is subnormal (m * 2^-9); the pattern with all
+ *   exponent and mantissa bits set is NaN; largest finite 448.
+ * fmt ORC_Q_INT8: the byte as a two's-complement integer.
+ * The decoded pool then goes through the float64 attention above unchanged.
+ * ---------------------------------------------------------------------------- */
+#define ORC_Q_E4M3 0
+#define ORC_Q_INT8 1
+
+static double decode_e4m3(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+int oracle_dequant_kv(const uint8_t* codes, const float* scales, int fmt, int64_t num_pages,
+                      int page_size, int num_kv_heads, int head_dim, double* out) {
+  if (num_pages < 0 || page_size <= 0 || num_kv_heads <= 0 || head_dim <= 0) return ORC_E_ARG;
+  if (fmt != ORC_Q_E4M3 && fmt != ORC_Q_INT8) return ORC_E_ARG;
+  for (int64_t pg = 0; pg < num_pages; ++pg)
+    for (int t = 0; t < page_size; ++t)
+      for (int h = 0; h < num_kv_heads; ++h) {
+        const double sc = (double)scales[((size_t)pg * num_kv_heads + h) * page_size + t];
+        const size_t base = (((size_t)pg * page_size + t) * num_kv_heads + h) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+          const uint8_t c = codes[base + d];
+          const double x = fmt == ORC_Q_E4M3 ? decode_e4m3(c) : (double)(int8_t)c;
+          out[base + d] = sc * x;
+        }
+      }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------
  * Philox4x32-10 (Salmon et al., SC'11): ten rounds of the 4x32 Philox S-box on a
  * 128-bit counter under a 64-bit key, the key advanced by the two Weyl constants
  * between rounds.

@@ -24,11 +24,18 @@ Five workloads (named by what they are, counted from 0):
                   log-normal lengths (median 2048, sigma 1.2) clamped to [256, 32768];
                   448 decode + 64 verify with k=4; spec_verify over vocab 128256, seed 99.
 
-and one beyond them, for chunked prefill:
+and beyond them, for chunked prefill:
 
 * ``prefill8``  - 8 sequences of context 4096, each bringing a 1024-token prompt chunk
                   (query length 1024, causal within the chunk), 70B attention shape,
-                  bf16, page 32; no spec_verify.
+                  bf16, page 32; no spec_verify;
+
+and for quantised KV pages, the 70B batch and decode64 with the same lengths, seeds and
+spec_verify, their K/V stored as FP8 E4M3 or INT8 codes with one fp32 scale per
+(token, KV head) for K and one for V (``stress70b_fp8``, ``stress70b_int8``,
+``decode64_fp8``, ``decode64_int8``).  The codes come from the same N(0, 1) draws:
+scale = max |x| over the head's D values / 448 (E4M3) or / 127 (INT8), code = x / scale
+rounded to nearest (E4M3 by torch's float8_e4m3fn conversion).
 
 Distributions (the pages leave them open; readings stated in the design doc): N(0, s) means
 standard deviation s; log-normal L = round(exp(ln median + sigma z)); Pareto
@@ -48,6 +55,9 @@ import torch
 
 F32 = "f32"
 BF16 = "bf16"
+FP8 = "fp8"    # K/V pages as FP8 E4M3 codes with a scale per (token, KV head); Q bf16
+INT8 = "int8"  # K/V pages as INT8 codes with a scale per (token, KV head); Q bf16
+QUANTIZED = (FP8, INT8)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -87,6 +97,10 @@ WORKLOADS = {
     "prefill8": Workload("prefill8", 7, 64, 8, 128, 32, BF16, "fixed", (), 8, 0, 0, 0,
                          fixed_lens=(4096,) * 8, fixed_qlens=(1024,) * 8),
 }
+for _base in ("stress70b", "decode64"):
+    for _q in QUANTIZED:
+        WORKLOADS[f"{_base}_{_q}"] = dataclasses.replace(WORKLOADS[_base], name=f"{_base}_{_q}",
+                                                         kv_dtype=_q)
 ORDER = ["tiny", "decode64", "verify32", "mixed272", "stress70b"]
 
 
@@ -147,7 +161,29 @@ def build_pool(lens: np.ndarray, page_size: int, seed: int, pool_pages: Optional
 
 
 def _torch_dtype(kv_dtype: str):
+    """Storage dtype of Q (and of K/V unless they are quantised)."""
     return torch.float32 if kv_dtype == F32 else torch.bfloat16
+
+
+def quantize_pool(x: torch.Tensor, kv_dtype: str):
+    """Codes and scales of a float pool [num_pages, P, Hkv, D]: one scale per (page,
+    slot, head), stored [num_pages, Hkv, P].  Returns (codes uint8, scales float32)."""
+    qmax = 448.0 if kv_dtype == FP8 else 127.0
+    n, P, H, D = x.shape
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((n, H, P), dtype=torch.float32, device=x.device)
+    step = max(1, (1 << 24) // max(1, P * H * D))
+    for s in range(0, n, step):
+        xs = x[s:s + step].float()
+        amax = xs.abs().amax(dim=-1)                                  # [n, P, H]
+        sc = torch.where(amax > 0, amax / qmax, torch.ones_like(amax))
+        y = (xs / sc[..., None]).clamp(-qmax, qmax)
+        if kv_dtype == FP8:
+            codes[s:s + step] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+        else:
+            codes[s:s + step] = y.round().to(torch.int8).view(torch.uint8)
+        scales[s:s + step] = sc.permute(0, 2, 1)
+    return codes, scales
 
 
 def normal_tensor(shape, seed: int, dtype, device="cpu") -> torch.Tensor:
@@ -178,6 +214,8 @@ class AttentionInputs:
     head_dim: int
     page_size: int
     kv_dtype: str
+    k_scale: Optional[torch.Tensor] = None  # float32 [num_pages, Hkv, P] (quantised pools)
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def num_seqs(self) -> int:
@@ -201,14 +239,21 @@ def attention_inputs(lens, qlens, *, num_q_heads, num_kv_heads, head_dim, page_s
     bt, num_pages = build_pool(lens, page_size, seed, pool_pages)
     dt = _torch_dtype(kv_dtype)
     shape = (num_pages, page_size, num_kv_heads, head_dim)
-    k_pages = normal_tensor(shape, seed * 4 + 1, dt, pool_device)
-    v_pages = normal_tensor(shape, seed * 4 + 2, dt, pool_device)
+    k_scale = v_scale = None
+    if kv_dtype in QUANTIZED:
+        k_pages, k_scale = quantize_pool(normal_tensor(shape, seed * 4 + 1, torch.float32,
+                                                       pool_device), kv_dtype)
+        v_pages, v_scale = quantize_pool(normal_tensor(shape, seed * 4 + 2, torch.float32,
+                                                       pool_device), kv_dtype)
+    else:
+        k_pages = normal_tensor(shape, seed * 4 + 1, dt, pool_device)
+        v_pages = normal_tensor(shape, seed * 4 + 2, dt, pool_device)
     T = int(qlens.sum())
     q = normal_tensor((T, num_q_heads, head_dim), seed * 4 + 3, dt, "cpu")
     return AttentionInputs(q, k_pages, v_pages, torch.from_numpy(bt),
                            torch.from_numpy(lens.astype(np.int32)),
                            torch.from_numpy(qlens.astype(np.int32)), num_q_heads,
-                           num_kv_heads, head_dim, page_size, kv_dtype)
+                           num_kv_heads, head_dim, page_size, kv_dtype, k_scale, v_scale)
 
 
 def draft_tree_parents(qlens, seed: int, extra_roots: float = 0.0) -> np.ndarray:
