@@ -58,9 +58,12 @@ typedef struct CUstream_st* vas_stream_t; /* identical to cudaStream_t */
 #define VAS_DEV_RESIDUAL_FALLBACK 0x100 /* informational: a zero residual after a       */
                                         /* rejection; the token was drawn from p_j      */
 
-/* Storage types of q, k_pages, v_pages and out. */
+/* Storage types of k_pages and v_pages (and of q and out for VAS_F32 / VAS_BF16; with
+ * the quantised types q and out are bf16). */
 #define VAS_F32 0
 #define VAS_BF16 1
+#define VAS_FP8_E4M3 2 /* FP8 E4M3 codes + fp32 scales, paged_attn_fwd_quant only */
+#define VAS_INT8 3     /* INT8 codes + fp32 scales, paged_attn_fwd_quant only     */
 
 /* ==================================================================================
  * Paged decode / verify attention
@@ -91,7 +94,8 @@ typedef struct {
   int32_t page_size;         /* P: 16 or 32 tokens per page                           */
   int32_t num_pages;         /* physical pages in the pool                            */
   int32_t max_pages_per_seq; /* columns of block_table                                */
-  int32_t kv_dtype;          /* VAS_BF16 or VAS_F32 (q and out share it)              */
+  int32_t kv_dtype;          /* VAS_BF16 or VAS_F32 (q and out share it), or          */
+                             /* VAS_FP8_E4M3 / VAS_INT8 (q and out bf16)              */
   float scale;               /* softmax scale; 0 selects 1/sqrt(head_dim)             */
 } vas_attn_dims;
 
@@ -154,6 +158,41 @@ int paged_attn_fwd_tree(const void* q, const void* k_pages, const void* v_pages,
                         const int32_t* query_lens, const uint64_t* tree_mask, void* out,
                         float* lse, const vas_attn_dims* dims, void* workspace,
                         size_t workspace_bytes, vas_stream_t stream);
+
+/* paged_attn_fwd over a quantised KV cache.
+ *
+ * Defined by: "llm-inference-optimization-batching" (tempatgunting.com), section
+ * "Quantization and Precision Choices for KV" -- INT8 or FP8 KV pages with per-head or
+ * per-token scaling factors, separate for K and V, dequantised inside the attention
+ * kernel; "Continuous Batching and Speculative Decoding..." (syslabs.in), section "A
+ * tuning framework" (an FP8 KV cache to fit more blocks).
+ *
+ * dims->kv_dtype is VAS_FP8_E4M3 (OCP E4M3: bias 7, 3 mantissa bits, subnormals, no
+ * infinities, max 448) or VAS_INT8 (two's complement).  Element d of token slot t of
+ * page p, KV head h, stands for
+ *     k = k_scale[(p * num_kv_heads + h) * page_size + t] * code(k_pages[p][t][h][d])
+ * and likewise for v with v_scale: one scale per token and KV head, no zero point.
+ * k_pages     [num_pages, P, Hkv, D] device bytes (the pool layout), 16-byte aligned.
+ * v_pages     the same for V.
+ * k_scale     [num_pages, Hkv, P] device fp32, 16-byte aligned.
+ * v_scale     the same for V.  Scales of slots past a sequence's end are not used.
+ * q, out      [T, Hq, D] bf16.  lse, block_table, seq_lens, query_lens, workspace: as for
+ *             paged_attn_fwd (the workspace queries are the same for every kv_dtype).
+ * tree_mask   null (the causal window) or the draft-tree masks of paged_attn_fwd_tree.
+ * Arithmetic: the codes are exact in f16; Q is taken to f16 (scaled by a power of two
+ * when its magnitude nears the f16 range), products accumulate in fp32, and P enters
+ * the PV product as f16 after multiplication by the V scale of its token, so
+ * |v_scale| * 256 must stay within the f16 range (|v| up to about 1e5).
+ * Errors: those of paged_attn_fwd; a kv_dtype that is not quantised, or a null scale
+ * array, is VAS_E_INVALID_ARG.  paged_attn_fwd and paged_attn_fwd_tree reject the
+ * quantised kv_dtypes with VAS_E_INVALID_ARG.
+ */
+int paged_attn_fwd_quant(const void* q, const void* k_pages, const void* v_pages,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* query_lens,
+                         const uint64_t* tree_mask, void* out, float* lse,
+                         const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
+                         vas_stream_t stream);
 
 /* paged_attn_fwd without a workspace argument, for callers that cannot allocate device
  * memory: code being captured into a CUDA graph (where cudaMalloc is not allowed), hosts

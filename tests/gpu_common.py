@@ -16,6 +16,8 @@ from verify_attention_spec_gb300 import workloads as wl
 # that half spacing plus the 2e-3 the computation is allowed below 4 (1e-2 - 2^-7).
 TOL = {wl.BF16: dict(max_abs=1e-2, rel_l2=5e-3, lse=2e-3, format_slack=2e-3),
        wl.F32: dict(max_abs=1e-5, rel_l2=1e-5, lse=2e-5, format_slack=None)}
+# Quantised pools: the oracle decodes the same codes exactly, and the output is bf16.
+TOL[wl.FP8] = TOL[wl.INT8] = TOL[wl.BF16]
 
 
 def bf16_half_spacing(x: np.ndarray) -> np.ndarray:
@@ -25,37 +27,46 @@ def bf16_half_spacing(x: np.ndarray) -> np.ndarray:
 
 
 def to_device(a: wl.AttentionInputs, device="cuda") -> wl.AttentionInputs:
-    mv = lambda t: t.to(device, non_blocking=False).contiguous()
+    mv = lambda t: None if t is None else t.to(device, non_blocking=False).contiguous()
     return wl.AttentionInputs(mv(a.q), mv(a.k_pages), mv(a.v_pages), mv(a.block_table),
                               mv(a.seq_lens), mv(a.query_lens), a.num_q_heads, a.num_kv_heads,
-                              a.head_dim, a.page_size, a.kv_dtype)
+                              a.head_dim, a.page_size, a.kv_dtype, mv(a.k_scale), mv(a.v_scale))
 
 
-def run_gpu_attention(vas, a: wl.AttentionInputs, workspace_bytes=None, out=None, lse=None):
+def _quant(a: wl.AttentionInputs):
+    return a.kv_dtype if a.kv_dtype in wl.QUANTIZED else None
+
+
+def run_gpu_attention(vas, a: wl.AttentionInputs, workspace_bytes=None, out=None, lse=None,
+                      tree_masks=None):
+    """One attention call through the C ABI: paged_attn_fwd, paged_attn_fwd_tree (with
+    tree_masks) or paged_attn_fwd_quant (quantised pools)."""
     d = a.q.device
     if out is None:
         out = torch.empty_like(a.q)
     if lse is None:
         lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=d)
-    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
+    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens, quant=_quant(a))
     ws = vas.alloc_workspace(dims, device=d, nbytes=workspace_bytes)
-    vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens, out,
-                       lse, ws, dims=dims)
+    tm = None
+    if tree_masks is not None:
+        tm = torch.from_numpy(np.ascontiguousarray(tree_masks).view(np.int64)).to(d)
+    if _quant(a):
+        vas.paged_attn_fwd_quant(a.q, a.k_pages, a.v_pages, a.k_scale, a.v_scale, a.block_table,
+                                 a.seq_lens, a.query_lens, out, lse, ws, quant=_quant(a),
+                                 tree_mask=tm, dims=dims)
+    elif tm is not None:
+        vas.paged_attn_fwd_tree(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens,
+                                a.query_lens, tm, out, lse, ws, dims=dims)
+    else:
+        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
+                           out, lse, ws, dims=dims)
     torch.cuda.synchronize()
     return out, lse
 
 
 def run_gpu_attention_tree(vas, a: wl.AttentionInputs, masks: np.ndarray, workspace_bytes=None):
-    d = a.q.device
-    out = torch.empty_like(a.q)
-    lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=d)
-    tm = torch.from_numpy(np.ascontiguousarray(masks).view(np.int64)).to(d)
-    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
-    ws = vas.alloc_workspace(dims, device=d, nbytes=workspace_bytes)
-    vas.paged_attn_fwd_tree(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
-                            tm, out, lse, ws, dims=dims)
-    torch.cuda.synchronize()
-    return out, lse
+    return run_gpu_attention(vas, a, workspace_bytes=workspace_bytes, tree_masks=masks)
 
 
 def ancestor_masks(parents: np.ndarray, qlens) -> np.ndarray:
@@ -75,6 +86,13 @@ def ancestor_masks(parents: np.ndarray, qlens) -> np.ndarray:
 
 
 def oracle_attention(a: wl.AttentionInputs, parents=None):
+    np_ = lambda t: t.detach().cpu().contiguous().numpy()
+    if a.kv_dtype in wl.QUANTIZED:
+        fmt = oracle.Q_E4M3 if a.kv_dtype == wl.FP8 else oracle.Q_INT8
+        return oracle.paged_attn_quant(wl.bf16_bits(a.q.cpu()), np_(a.k_pages), np_(a.v_pages),
+                                       np_(a.k_scale), np_(a.v_scale), np_(a.block_table),
+                                       np_(a.seq_lens), np_(a.query_lens), fmt=fmt,
+                                       parents=parents)
     code = oracle.BF16 if a.kv_dtype == wl.BF16 else oracle.F32
     st = lambda t: wl.storage_for_oracle(t, a.kv_dtype)
     return oracle.paged_attn(st(a.q), st(a.k_pages), st(a.v_pages), a.block_table.cpu().numpy(),
@@ -127,10 +145,12 @@ def subset_inputs(a: wl.AttentionInputs, seqs) -> wl.AttentionInputs:
     for r, ids in enumerate(new_bt):
         btn[r, :len(ids)] = ids
     rows = torch.from_numpy(np.concatenate(q_rows)).to(a.q.device)
+    sc = lambda t: None if t is None else t[all_ids.to(t.device)].cpu()
     return wl.AttentionInputs(a.q[rows].cpu(), a.k_pages[all_ids].cpu(), a.v_pages[all_ids].cpu(),
                               torch.from_numpy(btn), torch.from_numpy(lens[seqs].astype(np.int32)),
                               torch.from_numpy(qlens[seqs].astype(np.int32)), a.num_q_heads,
-                              a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype), np.concatenate(q_rows)
+                              a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype, sc(a.k_scale),
+                              sc(a.v_scale)), np.concatenate(q_rows)
 
 
 def query_slice_inputs(a: wl.AttentionInputs, seq: int, j0: int, n: int):
@@ -146,10 +166,12 @@ def query_slice_inputs(a: wl.AttentionInputs, seq: int, j0: int, n: int):
     npg = (Ls + P - 1) // P
     ids = torch.from_numpy(bt[seq, :npg].astype(np.int64)).to(a.k_pages.device)
     rows = np.arange(row0 + j0, row0 + j0 + n)
+    sc = lambda t: None if t is None else t[ids.to(t.device)].cpu()
     sub = wl.AttentionInputs(a.q[torch.from_numpy(rows).to(a.q.device)].cpu(), a.k_pages[ids].cpu(),
                              a.v_pages[ids].cpu(), torch.arange(npg, dtype=torch.int32)[None, :],
                              torch.tensor([Ls], dtype=torch.int32), torch.tensor([n], dtype=torch.int32),
-                             a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
+                             a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype,
+                             sc(a.k_scale), sc(a.v_scale))
     return sub, rows
 
 

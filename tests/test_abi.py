@@ -18,7 +18,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["paged_attn_fwd", "paged_attn_fwd_tree", "paged_attn_workspace_size", "spec_verify", "vas_last_device_error",
+    for n in ["paged_attn_fwd", "paged_attn_fwd_tree", "paged_attn_fwd_quant",
+              "paged_attn_workspace_size", "spec_verify", "vas_last_device_error",
               "vas_pool_create", "vas_build_block_table", "vas_seq_rollback"]:
         assert n in names
 
@@ -83,6 +84,25 @@ def test_host_validation_without_launch(vas_lib):
     st = lib.paged_attn_fwd_tree(fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                  ctypes.byref(d), fake, 16, null)
     assert st == vas_lib.VAS_E_WORKSPACE
+    # quantised pools: only through paged_attn_fwd_quant, and only with both scale arrays
+    for kv in (vas_lib.VAS_FP8_E4M3, vas_lib.VAS_INT8):
+        dq = _dims(vas_lib, kv_dtype=kv)
+        assert vas_lib.paged_attn_workspace_size(dq) == vas_lib.paged_attn_workspace_size(d)
+        st = lib.paged_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(dq),
+                                fake, 1 << 30, null)
+        assert st == vas_lib.VAS_E_INVALID_ARG
+        st = lib.paged_attn_fwd_quant(fake, fake, fake, null, fake, fake, fake, fake, null, fake,
+                                      fake, ctypes.byref(dq), fake, 1 << 30, null)
+        assert st == vas_lib.VAS_E_INVALID_ARG
+        st = lib.paged_attn_fwd_quant(fake, fake, fake, fake, P((1 << 20) + 4), fake, fake, fake,
+                                      null, fake, fake, ctypes.byref(dq), fake, 1 << 30, null)
+        assert st == vas_lib.VAS_E_INVALID_ARG
+        st = lib.paged_attn_fwd_quant(fake, fake, fake, fake, fake, fake, fake, fake, null, fake,
+                                      fake, ctypes.byref(dq), fake, 16, null)
+        assert st == vas_lib.VAS_E_WORKSPACE
+    st = lib.paged_attn_fwd_quant(fake, fake, fake, fake, fake, fake, fake, fake, null, fake, fake,
+                                  ctypes.byref(d), fake, 1 << 30, null)
+    assert st == vas_lib.VAS_E_INVALID_ARG  # bf16 pools take no scales
     # spec_verify argument checks
     assert lib.spec_verify(fake, fake, fake, 1, fake, fake, 4, 3, 0, null) == vas_lib.VAS_E_INVALID_ARG
     assert lib.spec_verify(null, fake, fake, 1, fake, fake, 4, 3, 10, null) == vas_lib.VAS_E_INVALID_ARG

@@ -41,6 +41,8 @@ VAS_DEV_TIMEOUT = 0x10
 VAS_DEV_RESIDUAL_FALLBACK = 0x100
 VAS_F32 = 0
 VAS_BF16 = 1
+VAS_FP8_E4M3 = 2
+VAS_INT8 = 3
 
 _c_void_p, _i32, _i64, _u32, _u64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                                                   ctypes.c_uint32, ctypes.c_uint64, ctypes.c_float,
@@ -60,6 +62,7 @@ _sig = {
     "paged_attn_workspace_min": ([_P_dims], _sz),
     "paged_attn_fwd": ([_c_void_p] * 8 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
     "paged_attn_fwd_tree": ([_c_void_p] * 9 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
+    "paged_attn_fwd_quant": ([_c_void_p] * 11 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
     "spec_verify": ([_c_void_p, _c_void_p, _c_void_p, _u64, _c_void_p, _c_void_p, _i32, _i32, _i32,
                      _c_void_p], ctypes.c_int),
     "vas_last_device_error": ([ctypes.POINTER(_i32), _c_void_p], ctypes.c_int),
@@ -116,20 +119,30 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> ctypes.c_void_p:
 _KV_CODES = {torch.bfloat16: VAS_BF16, torch.float32: VAS_F32}
 
 
+_QUANT_CODES = {"fp8": VAS_FP8_E4M3, "int8": VAS_INT8}
+
+
 def attn_dims(q: torch.Tensor, k_pages: torch.Tensor, block_table: torch.Tensor,
-              seq_lens: torch.Tensor, scale: float = 0.0) -> vas_attn_dims:
+              seq_lens: torch.Tensor, scale: float = 0.0, quant: Optional[str] = None) -> vas_attn_dims:
     """vas_attn_dims from tensor shapes: q [T, Hq, D], k_pages [num_pages, P, Hkv, D],
-    block_table [B, max_pages], seq_lens [B]."""
+    block_table [B, max_pages], seq_lens [B].  quant: None (k_pages share q's dtype), or
+    "fp8" / "int8" for a pool of 8-bit codes (uint8 tensors) with a bf16 q."""
     T, Hq, D = q.shape
     num_pages, P, Hkv, D2 = k_pages.shape
     if D2 != D:
         raise ValueError("head_dim of q and k_pages differ")
-    if q.dtype not in _KV_CODES or k_pages.dtype != q.dtype:
-        raise ValueError("q and k_pages must share a dtype in {bf16, fp32}")
+    if quant is not None:
+        if quant not in _QUANT_CODES or q.dtype != torch.bfloat16 or k_pages.dtype != torch.uint8:
+            raise ValueError("a quantised pool is uint8 codes with a bf16 q")
+        code = _QUANT_CODES[quant]
+    else:
+        if q.dtype not in _KV_CODES or k_pages.dtype != q.dtype:
+            raise ValueError("q and k_pages must share a dtype in {bf16, fp32}")
+        code = _KV_CODES[q.dtype]
     return vas_attn_dims(num_seqs=int(seq_lens.shape[0]), total_q_tokens=int(T), num_q_heads=int(Hq),
                          num_kv_heads=int(Hkv), head_dim=int(D), page_size=int(P),
                          num_pages=int(num_pages), max_pages_per_seq=int(block_table.shape[1]),
-                         kv_dtype=_KV_CODES[q.dtype], scale=float(scale))
+                         kv_dtype=code, scale=float(scale))
 
 
 def paged_attn_workspace_size(dims: vas_attn_dims) -> int:
@@ -181,6 +194,30 @@ def paged_attn_fwd_tree(q, k_pages, v_pages, block_table, seq_lens, query_lens, 
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream))
     _check("paged_attn_fwd_tree", st)
+
+
+def paged_attn_fwd_quant(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, query_lens,
+                         out, lse, workspace, *, quant: str, tree_mask=None, scale: float = 0.0,
+                         dims: Optional[vas_attn_dims] = None, stream=None) -> None:
+    """Attention over a quantised pool (include/vas.h: paged_attn_fwd_quant).  k_pages /
+    v_pages uint8 codes [num_pages, P, Hkv, D] ("fp8" E4M3 or "int8"); k_scale / v_scale
+    fp32 [num_pages, Hkv, P]; q and out bf16; tree_mask as for paged_attn_fwd_tree or None."""
+    if dims is None:
+        dims = attn_dims(q, k_pages, block_table, seq_lens, scale, quant=quant)
+    tm = ctypes.c_void_p(0)
+    if tree_mask is not None:
+        if tree_mask.numel() != q.shape[0]:
+            raise ValueError("tree_mask needs one word per query token")
+        tm = _dev(tree_mask, "tree_mask")
+    st = _lib.paged_attn_fwd_quant(
+        _dev(q, "q", torch.bfloat16), _dev(k_pages, "k_pages", torch.uint8),
+        _dev(v_pages, "v_pages", torch.uint8), _dev(k_scale, "k_scale", torch.float32),
+        _dev(v_scale, "v_scale", torch.float32), _dev(block_table, "block_table", torch.int32),
+        _dev(seq_lens, "seq_lens", torch.int32), _dev(query_lens, "query_lens", torch.int32), tm,
+        _dev(out, "out", torch.bfloat16), _dev(lse, "lse", torch.float32), ctypes.byref(dims),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream))
+    _check("paged_attn_fwd_quant", st)
 
 
 def spec_verify(p, q, draft_tokens, seed: int, accepted_len, out_tokens, *, stream=None) -> None:

@@ -57,12 +57,21 @@ namespace vas {
 namespace attn {
 
 constexpr int kStageTokens = 32;   // KV tokens per pipeline stage
-constexpr int kSlots = 8;          // stages in the shared-memory ring
 constexpr int kConsumerWarps = 4;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;      // TMA loads
 constexpr int kMmaWarp = kConsumerWarps + 1;       // tcgen05 issue for wide units
 constexpr int kThreads = kConsumerThreads + 64;    // + producer warp + MMA warp
+// Quantised KV pages (FP8 E4M3 or INT8 codes with fp32 scales per token and KV head):
+// the producer lands the codes and scales of a stage in a landing ring, and two
+// converter warps expand the codes into f16 stages of the same layout as bf16 stages.
+// Every product of such a call runs in f16 (codes exact; Q scaled into f16 range by a
+// power of two per unit; P in f16).
+constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvInt8 = 2;
+constexpr int kConvWarps = 2;
+constexpr int kConvWarp0 = kMmaWarp + 1;
+constexpr int kThreadsQ = kThreads + 32 * kConvWarps;
+constexpr int kLandSlots = 6;  // a multiple of kConvWarps (each converter keeps its slots)
 constexpr int kTmemCols = 256;
 constexpr int kTmemS = 0;    // S of a prompt-chunk stage, two 32-column buffers
 constexpr int kTmemO = 64;   // O: 128 lanes x D fp32
@@ -73,12 +82,7 @@ constexpr int kRowBlockTc = 128;   // ... or, for sequences with more rows (prom
 __host__ __device__ __forceinline__ int row_block(int R) {
   return R > kRowBlock ? kRowBlockTc : kRowBlock;
 }
-// In a decode unit warp w consumes the stages s with s % kConsumerWarps == w and waits
-// on slot s % kSlots by phase parity.  The parity test is only sound if the slot's
-// previous fill was consumed by the same warp, i.e. if kSlots is a multiple of the
-// number of consumer warps; otherwise a warp could pass the parity test while the
-// slot's previous fill is still in flight.
-static_assert(kSlots % kConsumerWarps == 0, "stage slots must be a multiple of the consumer warps");
+static_assert(kLandSlots % kConvWarps == 0, "landing slots must be a multiple of the converters");
 constexpr int kNarrowRows = 16;    // units with at most this many rows take the K Q^T form
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
@@ -425,10 +429,20 @@ struct AttnArgs {
   float scale;
   int32_t* err;
   const uint64_t* tree_mask;  // draft-tree visibility per query token, or null (causal)
+  const float* k_scale;       // quantised pools: [num_pages, Hkv, P] fp32
+  const float* v_scale;
 };
 
-template <int D>
+template <int D, int KQ = kKvBf16>
 struct Smem {
+  // Stages in the 16-bit ring.  In a decode unit warp w consumes the stages s with
+  // s % kConsumerWarps == w and waits on slot s % kSlots by phase parity.  The parity
+  // test is only sound if the slot's previous fill was consumed by the same warp, i.e.
+  // if kSlots is a multiple of the number of consumer warps; otherwise a warp could pass
+  // the parity test while the slot's previous fill is still in flight.  Quantised pools
+  // keep fewer 16-bit stages: their landing ring holds the stages in flight.
+  static constexpr int kSlots = KQ == kKvBf16 ? 8 : 4;
+  static_assert(kSlots % kConsumerWarps == 0, "stage slots must be a multiple of the consumer warps");
   static constexpr int NH = D / 64;                        // 128-byte halves per token row
   static constexpr int kRowBytes = D * 2;
   static constexpr int kOperandBytes = kStageTokens * kRowBytes;  // K or V of one stage
@@ -454,17 +468,27 @@ struct Smem {
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
-  static constexpr int kBarOff = kRingOff + kRing * (int)sizeof(RingEntry);
+  // Quantised pools: the landing ring (per slot the stage's K codes [32][D] bytes, V
+  // codes, 32 K scales, 32 V scales) and the scales of each 16-bit stage (32 K, 32 V).
+  static constexpr int kNLand = KQ == kKvBf16 ? 0 : kLandSlots;
+  static constexpr int kLandCodes = kStageTokens * D;
+  static constexpr int kLandStride = ((2 * kLandCodes + 2 * kStageTokens * 4 + 127) / 128) * 128;
+  static constexpr int kLandOff = kRingOff + kRing * (int)sizeof(RingEntry);
+  static constexpr int kScaleOff = kLandOff + kNLand * kLandStride;
+  static constexpr int kBarOff = kScaleOff + (kNLand ? kSlots * 2 * kStageTokens * 4 : 0);
   // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing], tensor-memory unit
-  // barriers bp[2], bo[2], bs[2], bq, bfin | meta[kSlots], flag[4], tmem base
+  // barriers bp[2], bo[2], bs[2], bq, bfin, landing lfull[kNLand], lempty[kNLand] |
+  // meta[kSlots], flag[4], tmem base, qmax[4], lmeta[kNLand]
   static constexpr int kWideBars = 8;
-  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars) * 8 + (kSlots + 4 + 1) * 4;
+  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars + 2 * kNLand) * 8 +
+                                   (kSlots + 4 + 1 + 4 + kNLand) * 4;
   // Draft-tree masks of the unit's rows (row r: its token's mask, own bit set).
   static constexpr int kTmaskOff = ((kBarOff + kBarBytes + 7) / 8) * 8;
   static constexpr int kBytes = kTmaskOff + kRowBlockTc * 8;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kDynBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(kPLoOff % 1024 == 0 && kQTileOff % 1024 == 0, "swizzle atoms of the tiles");
+  static_assert(kLandOff % 128 == 0 && kLandStride % 128 == 0, "landing slots");
 };
 
 // Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage.
@@ -508,8 +532,33 @@ __device__ __forceinline__ void narrow_offsets(int lane, uint32_t (&koff)[4], ui
   }
 }
 
+// ---- the 16-bit element type of a call: bf16, or f16 for quantised pools -------------
+template <int KQ>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  if constexpr (KQ == kKvBf16) mma_bf16_16816(d, a, b0, b1);
+  else mma_f16_16816(d, a, b0, b1);
+}
+template <int KQ>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (KQ == kKvBf16) return pack_bf16x2(lo, hi);
+  else return pack_f16x2(lo, hi);
+}
+template <int KQ>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+  if constexpr (KQ == kKvBf16) {
+    lo = bf16_lo_f32(v);
+    hi = bf16_hi_f32(v);
+  } else {
+    f16x2_to_f32(v, lo, hi);
+  }
+}
+
 // ---- narrow units: S^T = K Q^T, one warp per stage -------------------------------
-template <int D, int P, int NN, bool MASKED>
+// Quantised pools (KQ): the stage holds the codes as f16; the scores are multiplied by
+// the K scale of their token (ks) and P by the V scale of its token (vs) before the
+// PV product, which then sums scale * code * p.
+template <int D, int P, int NN, bool MASKED, int KQ>
 __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int loaded,
                                              const uint32_t (&qb)[D / 16][NN][2],
                                              const uint32_t (&koff)[4],
@@ -517,7 +566,8 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
                                              float (&oT)[D / 16][NN][4], float (&mref)[NN][2],
                                              float (&l)[NN][2], int t_abs0,
                                              const int (&lim)[NN][2], float c, int lane,
-                                             const uint64_t* tm, int ctx_end) {
+                                             const uint64_t* tm, int ctx_end, const float* ks,
+                                             const float* vs) {
   constexpr uint32_t kTile = tok_off<D, P>(16);  // 16 token rows
   const int g = lane >> 2;
   float s[2][NN][4];
@@ -534,13 +584,21 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
         uint32_t a[4];
         ldsm_x4(kbase + koff[ks & 3] + half_off<P>(ks) + mt * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(acc[ks & 1][nn], a, qb[ks][nn][0], qb[ks][nn][1]);
+        for (int nn = 0; nn < NN; ++nn) mma16816<KQ>(acc[ks & 1][nn], a, qb[ks][nn][0], qb[ks][nn][1]);
       }
+    }
+    float ksc[2] = {1.f, 1.f};
+    if constexpr (KQ != kKvBf16) {
+      ksc[0] = ks[16 * mt + g];
+      ksc[1] = ks[16 * mt + g + 8];
     }
 #pragma unroll
     for (int nn = 0; nn < NN; ++nn)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[mt][nn][e] = acc[0][nn][e] + acc[1][nn][e];
+      for (int e = 0; e < 4; ++e) {
+        s[mt][nn][e] = acc[0][nn][e] + acc[1][nn][e];
+        if constexpr (KQ != kKvBf16) s[mt][nn][e] *= ksc[e >> 1];
+      }
   }
   if (MASKED) {
 #pragma unroll
@@ -626,17 +684,22 @@ __device__ __forceinline__ void narrow_stage(uint32_t kbase, uint32_t vbase, int
   for (int kk = 0; kk < 2; ++kk) {
     if (!MASKED || 16 * kk < loaded) {
       uint32_t pb[NN][2];
+      float vsc[2] = {1.f, 1.f};
+      if constexpr (KQ != kKvBf16) {
+        vsc[0] = vs[16 * kk + g];
+        vsc[1] = vs[16 * kk + g + 8];
+      }
 #pragma unroll
       for (int nn = 0; nn < NN; ++nn) {
-        pb[nn][0] = movmatrix_trans(pack_bf16x2(s[kk][nn][0], s[kk][nn][1]));
-        pb[nn][1] = movmatrix_trans(pack_bf16x2(s[kk][nn][2], s[kk][nn][3]));
+        pb[nn][0] = movmatrix_trans(pack2<KQ>(s[kk][nn][0] * vsc[0], s[kk][nn][1] * vsc[0]));
+        pb[nn][1] = movmatrix_trans(pack2<KQ>(s[kk][nn][2] * vsc[1], s[kk][nn][3] * vsc[1]));
       }
 #pragma unroll
       for (int dt = 0; dt < D / 16; ++dt) {
         uint32_t a[4];
         ldsm_x4_trans(vbase + voff[dt & 3] + half_off<P>(dt) + kk * kTile, a[0], a[1], a[2], a[3]);
 #pragma unroll
-        for (int nn = 0; nn < NN; ++nn) mma_bf16_16816(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
+        for (int nn = 0; nn < NN; ++nn) mma16816<KQ>(oT[dt][nn], a, pb[nn][0], pb[nn][1]);
       }
     }
   }
@@ -658,13 +721,15 @@ __device__ __forceinline__ void wide_offsets(int lane, uint32_t (&kw)[2]) {
 // rescaling, and P as bf16 into this warp's 16 rows of the step's P tile (prow: the tile
 // row of row g; byte 2 tt of a row before the swizzle).  alpha / rescale report a moved
 // reference maximum: O, held in TMEM, is rescaled by the caller.
-template <int D, int P, int NST>
+template <int D, int P, int NST, int KQ>
 __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid, bool masked,
                                             const uint32_t (&qa)[D / 16][4],
                                             const uint32_t (&kw)[2], float (&mref)[2],
                                             float (&l)[2], float (&alpha)[2], bool& rescale,
                                             int t_abs0, int limA, int limB, float c, int lane,
-                                            uint8_t* prow, const uint64_t* tmw, int ctx_end) {
+                                            uint8_t* prow, const uint64_t* tmw, int ctx_end,
+                                            const float* ks0, const float* ks1,
+                                            const float* vs0, const float* vs1) {
   constexpr int NT = 4 * NST;
   const int g = lane >> 2, tq = lane & 3;
   float s[NT][4];
@@ -680,9 +745,20 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
       uint32_t b0, b1, b2, b3;
       ldsm_x4(kb[nt >> 2] + kw[qd & 1] + half_off<P>(2 * qd) + tok_off<D, P>(8 * (nt & 3)), b0,
               b1, b2, b3);
-      mma_bf16_16816(s[nt], qa[2 * qd], b0, b1);
-      mma_bf16_16816(s[nt], qa[2 * qd + 1], b2, b3);
+      mma16816<KQ>(s[nt], qa[2 * qd], b0, b1);
+      mma16816<KQ>(s[nt], qa[2 * qd + 1], b2, b3);
     }
+  // Quantised pools: token tt's scores times its K scale (stage tt / 32).
+  if constexpr (KQ != kKvBf16) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float2 k2 = *reinterpret_cast<const float2*>((nt < 4 ? ks0 : ks1) + 8 * (nt & 3) + 2 * tq);
+      s[nt][0] *= k2.x;
+      s[nt][1] *= k2.y;
+      s[nt][2] *= k2.x;
+      s[nt][3] *= k2.y;
+    }
+  }
   if (masked) {
     // Draft tree: rows g and g + 8 keep only their ancestors (and themselves) among the
     // draft tokens (positions from ctx_end on).
@@ -730,9 +806,16 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
       p[e] = ex2_approx(fmaf(s[nt][e], c, nm[e >> 1]));
       l[e >> 1] += p[e];
     }
+    if constexpr (KQ != kKvBf16) {  // P times the V scale of its token
+      const float2 v2 = *reinterpret_cast<const float2*>((nt < 4 ? vs0 : vs1) + 8 * (nt & 3) + 2 * tq);
+      p[0] *= v2.x;
+      p[1] *= v2.y;
+      p[2] *= v2.x;
+      p[3] *= v2.y;
+    }
     const int off = ((nt ^ g) << 4) + 4 * tq;
-    *reinterpret_cast<uint32_t*>(prow + off) = pack_bf16x2(p[0], p[1]);
-    *reinterpret_cast<uint32_t*>(prow + 8 * 128 + off) = pack_bf16x2(p[2], p[3]);
+    *reinterpret_cast<uint32_t*>(prow + off) = pack2<KQ>(p[0], p[1]);
+    *reinterpret_cast<uint32_t*>(prow + 8 * 128 + off) = pack2<KQ>(p[2], p[3]);
   }
 }
 
@@ -742,23 +825,32 @@ __device__ __forceinline__ void wide_s_step(const uint32_t (&kb)[2], int tvalid,
 // tile (K-major, 128-byte swizzle); tokens outside `valid` get 0.  Returns the row's sum
 // of P.  A precise unit also writes each value's bf16 rounding error into the low tile
 // (O += P_lo V follows O += P V).
-template <int D, bool PRECISE>
+// Quantised pools: the scores sr are already scaled by their tokens' K scales, and P
+// is multiplied by the V scale of its token (vs) before it is written (the sum is of P
+// itself).
+template <int D, bool PRECISE, int KQ>
 __device__ __forceinline__ float chunk_p_row(const uint32_t (&sr)[32], uint32_t valid, float c,
-                                             float mu, uint8_t* prow, int r) {
+                                             float mu, uint8_t* prow, int r, const float* vs) {
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
   uint32_t hw[16];
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const float e0 = ex2_approx(fmaf(__uint_as_float(sr[i]), c, -mu));
     const float e1 = ex2_approx(fmaf(__uint_as_float(sr[i + 1]), c, -mu));
-    const float p0 = (valid >> i) & 1 ? e0 : 0.f;
-    const float p1 = (valid >> (i + 1)) & 1 ? e1 : 0.f;
-    const uint32_t h = pack_bf16x2(p0, p1);
-    hw[i >> 1] = h;
+    float p0 = (valid >> i) & 1 ? e0 : 0.f;
+    float p1 = (valid >> (i + 1)) & 1 ? e1 : 0.f;
     s4[(i >> 1) & 3] += p0 + p1;
+    if constexpr (KQ != kKvBf16) {
+      p0 *= vs[i];
+      p1 *= vs[i + 1];
+    }
+    const uint32_t h = pack2<KQ>(p0, p1);
+    hw[i >> 1] = h;
     if constexpr (PRECISE) {
       // The low part goes out at once: its 16 words are never live together.
-      const uint32_t lo = pack_bf16x2(p0 - bf16_lo_f32(h), p1 - bf16_hi_f32(h));
+      float h0, h1;
+      unpack2<KQ>(h, h0, h1);
+      const uint32_t lo = pack2<KQ>(p0 - h0, p1 - h1);
       *reinterpret_cast<uint32_t*>(prow + (Smem<D>::kPLoOff - Smem<D>::kPTileOff) +
                                    (((i >> 3) ^ (r & 7)) << 4) + (i & 7) * 2) = lo;
     }
@@ -768,6 +860,26 @@ __device__ __forceinline__ float chunk_p_row(const uint32_t (&sr)[32], uint32_t 
     *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
         make_uint4(hw[4 * ch], hw[4 * ch + 1], hw[4 * ch + 2], hw[4 * ch + 3]);
   return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
+// ---- quantised pools: the unit's Q in f16 ----------------------------------------------
+// Largest magnitude of eight bf16 values.
+__device__ __forceinline__ float absmax_bf16x8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = fmaxf(m, fmaxf(fabsf(bf16_lo_f32(w[i])), fabsf(bf16_hi_f32(w[i]))));
+  return m;
+}
+// Eight bf16 values times mul (a power of two), as f16 (exact unless below the f16
+// normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float mul) {
+  uint4 r;
+  r.x = pack_f16x2(bf16_lo_f32(v.x) * mul, bf16_hi_f32(v.x) * mul);
+  r.y = pack_f16x2(bf16_lo_f32(v.y) * mul, bf16_hi_f32(v.y) * mul);
+  r.z = pack_f16x2(bf16_lo_f32(v.z) * mul, bf16_hi_f32(v.z) * mul);
+  r.w = pack_f16x2(bf16_lo_f32(v.w) * mul, bf16_hi_f32(v.w) * mul);
+  return r;
 }
 
 // ---- unit classification ------------------------------------------------------------
@@ -884,13 +996,17 @@ __device__ __forceinline__ void finish_pending(const AttnArgs& a, PendingMerge& 
   pm.valid = 0;
 }
 
-template <int D, int P>
-__global__ void __launch_bounds__(kThreads, 1)
+// KQ: kKvBf16 (bf16 pages, tm_k / tm_v over the pool) or kKvFp8 / kKvInt8 (8-bit codes,
+// tm_k / tm_v over the code pools, scales in a.k_scale / a.v_scale).
+template <int D, int P, int KQ>
+__global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const AttnArgs a) {
-  using S = Smem<D>;
+  using S = Smem<D, KQ>;
+  constexpr bool kQuant = KQ != kKvBf16;
+  constexpr int kSlots = S::kSlots;
   constexpr int PPS = kStageTokens / P;  // pages per stage
-  constexpr int kPageBytes = P * D * 2;  // one page of one head, one operand
+  constexpr int kPageBytes = P * D * 2;  // one page of one head, one operand (16-bit)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -910,9 +1026,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bs = bo + 2;
   uint64_t* bq = bs + 2;
   uint64_t* bfin = bq + 1;
-  int32_t* meta = reinterpret_cast<int32_t*>(bfin + 1);
+  uint64_t* lfull = bfin + 1;  // landing ring (quantised pools)
+  uint64_t* lempty = lfull + S::kNLand;
+  int32_t* meta = reinterpret_cast<int32_t*>(lempty + S::kNLand);
   int32_t* flag = meta + kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flag + 4);
+  float* qmax = reinterpret_cast<float*>(tmem_slot + 1);
+  int32_t* lmeta = reinterpret_cast<int32_t*>(qmax + 4);
+  uint8_t* land = smem + S::kLandOff;
+  float* stage_scales = reinterpret_cast<float*>(smem + S::kScaleOff);  // [kSlots][K 32 | V 32]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -922,7 +1044,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&ufull[r], 1);
-      mbar_init(&uempty[r], kConsumerWarps + 1);  // consumers and the MMA warp
+      // consumers, the MMA warp and (quantised pools) the converters
+      mbar_init(&uempty[r], kConsumerWarps + 1 + (kQuant ? kConvWarps : 0));
+    }
+    for (int s = 0; s < S::kNLand; ++s) {
+      mbar_init(&lfull[s], 1);
+      mbar_init(&lempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bp[b], kConsumerWarps);
@@ -1015,8 +1142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t my_id =
               pg0 == it.page_begin ? bt_cur : (lane < npg ? bt_row[pg0 + lane] : 0);
           for (int s0 = 0; s0 < npg; s0 += PPS) {
-            const int slot_s = stage_it % kSlots;
-            ok = mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1);
+            // bf16: the stage goes to 16-bit slot stage % kSlots; quantised: to landing
+            // slot stage % kLandSlots, which a converter empties.
+            const int slot_s = kQuant ? stage_it % kLandSlots : stage_it % kSlots;
+            ok = kQuant ? mbar_wait(&lempty[slot_s], ((stage_it / kLandSlots) & 1) ^ 1)
+                        : mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1);
             if (!ok) break;
             const int n_in = min(PPS, npg - s0);
             int ids[PPS];
@@ -1027,10 +1157,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               ids[e] = __shfl_sync(0xffffffffu, my_id, (s0 + e) & 31);
               if (e < n_in) {
                 if (ids[e] < 0 || ids[e] >= a.num_pages) bad = 1;
-                else bytes += 2u * kPageBytes;
+                else bytes += kQuant ? 2u * (P * D + P * 4) : 2u * kPageBytes;
               }
             }
-            if (lane == 0) {
+            if (kQuant && lane == 0) {
+              // Codes: one box per page and operand, [P tokens][D bytes]; scales: P
+              // floats per page, head and operand, contiguous in [page][head][slot].
+              lmeta[slot_s] = bad;
+              mbar_arrive_expect_tx(&lfull[slot_s], bytes);
+              uint8_t* kdst = land + slot_s * S::kLandStride;
+              uint8_t* vdst = kdst + S::kLandCodes;
+              float* ksd = reinterpret_cast<float*>(vdst + S::kLandCodes);
+              float* vsd = ksd + kStageTokens;
+#pragma unroll
+              for (int e = 0; e < PPS; ++e) {
+                if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
+                  tma_load_3d(kdst + e * P * D, &tm_k, &lfull[slot_s], 0, ids[e] * P, head, pol);
+                  tma_load_3d(vdst + e * P * D, &tm_v, &lfull[slot_s], 0, ids[e] * P, head, pol);
+                  const size_t so = ((size_t)ids[e] * a.Hkv + head) * P;
+                  bulk_load(ksd + e * P, a.k_scale + so, P * 4, &lfull[slot_s], pol);
+                  bulk_load(vsd + e * P, a.v_scale + so, P * 4, &lfull[slot_s], pol);
+                }
+              }
+            }
+            if (!kQuant && lane == 0) {
               meta[slot_s] = bad;
               mbar_arrive_expect_tx(&full[slot_s], bytes);
               uint8_t* kdst = stages + slot_s * S::kStageBytes;
@@ -1062,8 +1212,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
     pdl_launch_dependents();  // no more work for this CTA: the next kernel may launch
     // Let every copy this warp issued land before the CTA can exit.
-    for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
-      mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
+    if constexpr (kQuant) {
+      for (uint32_t d = stage_it > kLandSlots ? stage_it - kLandSlots : 0; d < stage_it; ++d)
+        mbar_wait(&lfull[d % kLandSlots], (d / kLandSlots) & 1);
+    } else {
+      for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
+        mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
+    }
+    return;
+  }
+
+  if (kQuant && warp >= kConvWarp0) {
+    // ------------------------------ converters ------------------------------
+    // Follow the unit ring.  Converter c takes the stages s with s % kConvWarps == c:
+    // it waits for landing slot s % kLandSlots and for 16-bit slot s % kSlots to be
+    // free, expands the codes to f16 in the bf16 stage layout, copies the stage's
+    // scales (zero past the loaded tokens and past the sequence end, where the pool
+    // may hold anything), and arrives on the stage's full barrier.  Both ring sizes are
+    // multiples of kConvWarps, so each converter waits only on slots it used last.
+    const int cw = warp - kConvWarp0;
+    uint32_t stage_it = 0, unit_it = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = unit_it % kRing;
+      if (!mbar_wait(&ufull[slot], (unit_it / kRing) & 1)) {
+        ok = false;
+        break;
+      }
+      const RingEntry re = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&uempty[slot]);
+      ++unit_it;
+      if (re.u < 0) break;
+      const Item it = re.item;
+      if (it.seq < 0) continue;
+      const int L = re.sp.len;
+      const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
+      for (int si = 0; si < n_stages; ++si, ++stage_it) {
+        if ((int)(stage_it % kConvWarps) != cw) continue;
+        const int ls = stage_it % kLandSlots, slot_s = stage_it % kSlots;
+        if (!mbar_wait(&lfull[ls], (stage_it / kLandSlots) & 1) ||
+            !mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        const int pg = it.page_begin + si * PPS;
+        const int loaded = min(PPS, it.page_end - pg) * P;
+        const int t_abs0 = pg * P;
+        const uint8_t* lk = land + ls * S::kLandStride;
+        const uint8_t* lv = lk + S::kLandCodes;
+        const float* lks = reinterpret_cast<const float*>(lv + S::kLandCodes);
+        uint8_t* kt = stages + slot_s * S::kStageBytes;
+        uint8_t* vt = kt + S::kOperandBytes;
+        constexpr int kC = D / 16;  // 16-code chunks per token row
+        for (int c = lane; c < loaded * kC; c += 32) {
+          const int t = c / kC, ch = c % kC;
+#pragma unroll
+          for (int op = 0; op < 2; ++op) {
+            const uint4 x = *reinterpret_cast<const uint4*>((op ? lv : lk) + t * D + ch * 16);
+            uint4 y0, y1;
+            if constexpr (KQ == kKvFp8) {
+              e4m3x4_to_f16x4(x.x, y0.x, y0.y);
+              e4m3x4_to_f16x4(x.y, y0.z, y0.w);
+              e4m3x4_to_f16x4(x.z, y1.x, y1.y);
+              e4m3x4_to_f16x4(x.w, y1.z, y1.w);
+            } else {
+              s8x4_to_f16x4(x.x, y0.x, y0.y);
+              s8x4_to_f16x4(x.y, y0.z, y0.w);
+              s8x4_to_f16x4(x.z, y1.x, y1.y);
+              s8x4_to_f16x4(x.w, y1.z, y1.w);
+            }
+            uint8_t* dst = op ? vt : kt;
+            *reinterpret_cast<uint4*>(dst + kv_off<D, P>(t, 2 * ch)) = y0;
+            *reinterpret_cast<uint4*>(dst + kv_off<D, P>(t, 2 * ch + 1)) = y1;
+          }
+        }
+        {
+          const bool live = lane < loaded && t_abs0 + lane < L;
+          float* sc = stage_scales + slot_s * 2 * kStageTokens;
+          sc[lane] = live ? lks[lane] : 0.f;
+          sc[kStageTokens + lane] = live ? lks[kStageTokens + lane] : 0.f;
+        }
+        if (lane == 0) meta[slot_s] = lmeta[ls];
+        fence_proxy_async_smem();  // tcgen05 reads these stages as operands
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&lempty[ls]);
+          mbar_arrive(&full[slot_s]);
+        }
+      }
+      if (!ok) break;
+    }
+    if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
     return;
   }
 
@@ -1079,8 +1319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (bs, the S buffers); wq: prompt-chunk units (bq).
     uint32_t stage_it = 0, unit_it = 0, wk = 0, wc = 0, wq = 0;
     bool ok = true;
-    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, false, true);
-    constexpr uint32_t kIdS = umma_idesc_bf16(128, P == 32 ? 32 : 16, false, false);
+    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, false, true, kQuant);
+    constexpr uint32_t kIdS = umma_idesc_bf16(128, P == 32 ? 32 : 16, false, false, kQuant);
     // All operands are 128-byte swizzled with 1024-byte 8-row groups: the high descriptor
     // word is shared, the low word carries the start address.
     constexpr uint32_t kDescHi = umma_desc_hi_sw128(1024);
@@ -1291,6 +1531,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Prompt-chunk and precise row blocks: tcgen05 S and PV, rows in TMEM lanes.
     const bool chunk = (RB == kRowBlockTc || precise) && n_stages > 0;
     const bool wide = !chunk && Rb > kNarrowRows && n_stages > 0;
+    // Quantised pools: Q goes to f16 times qmul = 2^-e, the power of two that brings
+    // the unit's largest |q| under 2^15 (1 for any ordinary Q), and the scores are
+    // scaled back through cunit.
+    float qmul = 1.f, cunit = a.scale_log2;
+    if constexpr (kQuant) {
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
+      float mx = 0.f;
+      for (int c = tid; c < Rb * (D / 8); c += kConsumerThreads)
+        mx = fmaxf(mx, absmax_bf16x8(*reinterpret_cast<const uint4*>(
+                           qg + out_row(a, sp, head, r0 + c / (D / 8)) * D + (c % (D / 8)) * 8)));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) qmax[warp] = mx;
+      named_bar_sync(1, kConsumerThreads);
+      const float m = fmaxf(fmaxf(qmax[0], qmax[1]), fmaxf(qmax[2], qmax[3]));
+      if (m > 32768.f && m <= 3.0e38f) {
+        int e;
+        frexpf(m, &e);  // m < 2^e
+        qmul = ldexpf(1.f, 15 - e);
+        cunit = ldexpf(a.scale_log2, e - 15);
+      }
+    }
     if (chunk) {
       // The query tile for tcgen05 S: rows 0 .. Rb-1 (row r: token r / G, head
       // head * G + r % G) in the K-major 128-byte-swizzled layout.  Rows past Rb keep
@@ -1300,9 +1562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* qt = scratch + S::kQTileOff;
       for (int c = tid; c < Rb * kChunks; c += kConsumerThreads) {
         const int row = c / kChunks, gc = c % kChunks;
+        uint4 v = *reinterpret_cast<const uint4*>(qg + out_row(a, sp, head, r0 + row) * D + gc * 8);
+        if constexpr (kQuant) v = bf16x8_to_f16x8(v, qmul);
         *reinterpret_cast<uint4*>(qt + (gc >> 3) * (128 * 128) + row * 128 +
-                                  (((gc & 7) ^ (row & 7)) << 4)) =
-            *reinterpret_cast<const uint4*>(qg + out_row(a, sp, head, r0 + row) * D + gc * 8);
+                                  (((gc & 7) ^ (row & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -1316,8 +1579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = tid; c < rows_pad * kChunks; c += kConsumerThreads) {
         const int row = c / kChunks, ch = c % kChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < Rb)
+        if (row < Rb) {
           v = *reinterpret_cast<const uint4*>(qg + out_row(a, sp, head, r0 + row) * D + ch * 8);
+          if constexpr (kQuant) v = bf16x8_to_f16x8(v, qmul);
+        }
         *reinterpret_cast<uint4*>(scratch + row * S::kQStride + ch * 16) = v;
       }
       named_bar_sync(1, kConsumerThreads);
@@ -1336,7 +1601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool warp_ok = 32 * warp < Rb;
       const int lim = row_ok ? L - ql + (r0 + r) / a.G : -1;
       const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-      const float c = a.scale_log2;
+      const float c = cunit;
       float mref = -INFINITY, l = 0.f;
       for (int si = 0; si < n_stages; ++si, ++stage_it) {
         const uint32_t k = wk + si, b = k & 1, kc = wc + si;
@@ -1368,6 +1633,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp_ok) {
           uint32_t sr[32];
           tmem_ld32(tmem + lane_base + kTmemS + (kc & 1) * 32, sr);
+          const float* kss = stage_scales + slot_s * 2 * kStageTokens;  // quantised pools
+          if constexpr (kQuant) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 k4 = *reinterpret_cast<const float4*>(kss + i);
+              sr[i] = __float_as_uint(__uint_as_float(sr[i]) * k4.x);
+              sr[i + 1] = __float_as_uint(__uint_as_float(sr[i + 1]) * k4.y);
+              sr[i + 2] = __float_as_uint(__uint_as_float(sr[i + 2]) * k4.z);
+              sr[i + 3] = __float_as_uint(__uint_as_float(sr[i + 3]) * k4.w);
+            }
+          }
           // Valid tokens of this row form a prefix of the stage: i < loaded, t <= lim.
           const int nv = row_ok ? max(0, min(loaded, lim - t_abs0 + 1)) : 0;
           uint32_t valid = nv >= 32 ? 0xffffffffu : (1u << nv) - 1u;
@@ -1407,8 +1683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float mu = mref == -INFINITY ? 0.f : mref;
           uint8_t* prow = scratch + S::kPTileOff + b * S::kPTileBytes + r * 128;
-          l += precise ? chunk_p_row<D, true>(sr, valid, c, mu, prow, r)
-                       : chunk_p_row<D, false>(sr, valid, c, mu, prow, r);
+          l += precise ? chunk_p_row<D, true, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens)
+                       : chunk_p_row<D, false, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens);
           fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -1524,12 +1800,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
           }
+          const float* kss = kQuant ? stage_scales + slot_s * 2 * kStageTokens : nullptr;
+          const float* vss = kQuant ? kss + kStageTokens : nullptr;
           if (loaded == kStageTokens && t_abs0 + kStageTokens - 1 <= min_lim)
-            narrow_stage<D, P, NN, false>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                          lim, a.scale_log2, lane, tm, ctx_end);
+            narrow_stage<D, P, NN, false, KQ>(kbase, vbase, loaded, qb, koff, voff, oT, m, l,
+                                              t_abs0, lim, cunit, lane, tm, ctx_end, kss, vss);
           else
-            narrow_stage<D, P, NN, true>(kbase, vbase, loaded, qb, koff, voff, oT, m, l, t_abs0,
-                                         lim, a.scale_log2, lane, tm, ctx_end);
+            narrow_stage<D, P, NN, true, KQ>(kbase, vbase, loaded, qb, koff, voff, oT, m, l,
+                                             t_abs0, lim, cunit, lane, tm, ctx_end, kss, vss);
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot_s]);
         }
@@ -1642,6 +1920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Both stages of the step are loaded (and their V rows past the sequence end
         // zeroed: those slots may hold anything, NaN included, and meet P = 0).
         uint32_t kb[2];
+        const float* ksp[2] = {nullptr, nullptr};  // quantised pools: the stages' scales
         int loaded = 0;
         bool got = true;
         const int t_abs0 = (it.page_begin + 2 * sj * PPS) * P;
@@ -1653,6 +1932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pg = it.page_begin + (2 * sj + h) * PPS;
           const int ld = min(PPS, it.page_end - pg) * P;
           kb[h] = smem_u32(stages + slot_s * S::kStageBytes);
+          ksp[h] = stage_scales + slot_s * 2 * kStageTokens;
           const int ta = pg * P;
           if (ta + ld > L) {
             uint8_t* vt = stages + slot_s * S::kStageBytes + S::kOperandBytes;
@@ -1664,7 +1944,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           loaded += ld;
         }
-        if (nst == 1) kb[1] = kb[0];
+        if (nst == 1) {
+          kb[1] = kb[0];
+          ksp[1] = ksp[0];
+        }
         if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
           timed_out = true;
           stage_it += n_stages - 2 * sj;
@@ -1684,11 +1967,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float alpha[2];
           bool rescale;
           if (nst == 2)
-            wide_s_step<D, P, 2>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
-                              limB, a.scale_log2, lane, prow, tmw, ctx_end);
+            wide_s_step<D, P, 2, KQ>(kb, loaded, masked, qa, kw, mref, l, alpha, rescale, t_abs0,
+                                     limA, limB, cunit, lane, prow, tmw, ctx_end, ksp[0], ksp[1],
+                                     ksp[0] + kStageTokens, ksp[1] + kStageTokens);
           else
-            wide_s_step<D, P, 1>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0, limA,
-                              limB, a.scale_log2, lane, prow, tmw, ctx_end);
+            wide_s_step<D, P, 1, KQ>(kb, loaded, true, qa, kw, mref, l, alpha, rescale, t_abs0,
+                                     limA, limB, cunit, lane, prow, tmw, ctx_end, ksp[0], ksp[1],
+                                     ksp[0] + kStageTokens, ksp[1] + kStageTokens);
           if (__any_sync(0xffffffffu, rescale && sj > 0)) {
             // O holds the products up to the previous step: wait for the last of them,
             // then scale row 16 w + t (lane t < 16) by its factor (held by lane 4 (t % 8)).
@@ -1901,7 +2186,12 @@ bool dims_ok(const vas_attn_dims* d) {
 
 bool dims_supported(const vas_attn_dims* d) {
   return (d->head_dim == 64 || d->head_dim == 128) && (d->page_size == 16 || d->page_size == 32) &&
-         (d->kv_dtype == VAS_BF16 || d->kv_dtype == VAS_F32);
+         (d->kv_dtype == VAS_BF16 || d->kv_dtype == VAS_F32 || d->kv_dtype == VAS_FP8_E4M3 ||
+          d->kv_dtype == VAS_INT8);
+}
+
+bool kv_quantized(const vas_attn_dims* d) {
+  return d->kv_dtype == VAS_FP8_E4M3 || d->kv_dtype == VAS_INT8;
 }
 
 int64_t items_min(const vas_attn_dims* d) {
@@ -1982,23 +2272,40 @@ bool encode_pool_map(CUtensorMap* map, const void* base, const vas_attn_dims* d)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int P>
+// 3-D view of an 8-bit code pool: (D bytes, num_pages * P tokens, Hkv), strides
+// (Hkv*D, D) bytes, no swizzle.  A box of (D, P, 1) -- one page of one KV head -- lands
+// as [P tokens][D bytes].
+bool encode_code_map(CUtensorMap* map, const void* base, const vas_attn_dims* d) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->num_pages * d->page_size,
+                              (cuuint64_t)d->num_kv_heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)d->num_kv_heads * d->head_dim,
+                                 (cuuint64_t)d->head_dim};
+  const cuuint32_t box[3] = {(cuuint32_t)d->head_dim, (cuuint32_t)d->page_size, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int P, int KQ>
 int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const AttnArgs& args, int grid,
                 cudaStream_t stream) {
-  using S = Smem<D>;
+  using S = Smem<D, KQ>;
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return VAS_E_CUDA;
   std::call_once(once[dev & 63], [&] {
-    attr_err[dev & 63] = cudaFuncSetAttribute(attn_bf16_kernel<D, P>,
+    attr_err[dev & 63] = cudaFuncSetAttribute(attn_bf16_kernel<D, P, KQ>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               S::kDynBytes);
   });
   if (attr_err[dev & 63] != cudaSuccess) return VAS_E_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(KQ == kKvBf16 ? kThreads : kThreadsQ);
   cfg.dynamicSmemBytes = S::kDynBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -2006,7 +2313,7 @@ int launch_bf16(const CUtensorMap& mk, const CUtensorMap& mv, const AttnArgs& ar
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, P>, mk, mv, args) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, attn_bf16_kernel<D, P, KQ>, mk, mv, args) != cudaSuccess) {
     cudaGetLastError();
     return VAS_E_CUDA;
   }
@@ -2038,13 +2345,17 @@ size_t paged_attn_workspace_size(const vas_attn_dims* dims) {
 
 namespace {
 
-int attn_launch(const void* q, const void* k_pages, const void* v_pages,
-                const int32_t* block_table, const int32_t* seq_lens, const int32_t* query_lens,
-                const uint64_t* tree_mask, void* out, float* lse, const vas_attn_dims* dims,
-                void* workspace, size_t workspace_bytes, vas_stream_t stream_) {
+int attn_launch(const void* q, const void* k_pages, const void* v_pages, const float* k_scale,
+                const float* v_scale, const int32_t* block_table, const int32_t* seq_lens,
+                const int32_t* query_lens, const uint64_t* tree_mask, void* out, float* lse,
+                const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
+                vas_stream_t stream_) {
   if (!dims_ok(dims)) return VAS_E_INVALID_ARG;
   if (!dims_supported(dims)) return VAS_E_UNSUPPORTED;
   const vas_attn_dims& d = *dims;
+  const bool quant = kv_quantized(dims);
+  // Quantised pools need their scales; the other storage types take none.
+  if (quant != (k_scale != nullptr) || quant != (v_scale != nullptr)) return VAS_E_INVALID_ARG;
   if (d.num_seqs == 0 || d.total_q_tokens == 0) return VAS_OK;
   if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !query_lens || !out || !lse ||
       !workspace)
@@ -2052,7 +2363,7 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages,
   auto mis = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
   if (mis(q, 16) || mis(k_pages, 16) || mis(v_pages, 16) || mis(out, 16) || mis(lse, 4) ||
       mis(block_table, 4) || mis(seq_lens, 4) || mis(query_lens, 4) || mis(workspace, 256) ||
-      mis(tree_mask, 8))
+      mis(tree_mask, 8) || mis(k_scale, 16) || mis(v_scale, 16))
     return VAS_E_INVALID_ARG;
   if (d.num_pages == 0 || d.max_pages_per_seq == 0) return VAS_E_INVALID_ARG;
   if ((int64_t)d.num_pages * d.page_size > INT32_MAX) return VAS_E_INVALID_ARG;
@@ -2066,7 +2377,7 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
   const int G = d.num_q_heads / d.num_kv_heads;
-  const bool bf16 = d.kv_dtype == VAS_BF16;
+  const bool bf16 = d.kv_dtype != VAS_F32;  // the tensor-core kernel; out and q are bf16
   PlanArgs pa;
   pa.seq_lens = seq_lens;
   pa.query_lens = query_lens;
@@ -2137,16 +2448,37 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages,
   aa.scale_log2 = scale * 1.4426950408889634f;
   aa.err = err;
   aa.tree_mask = tree_mask;
+  aa.k_scale = k_scale;
+  aa.v_scale = v_scale;
 
+  if (quant) {
+    CUtensorMap mk, mv;
+    if (!encode_code_map(&mk, k_pages, dims) || !encode_code_map(&mv, v_pages, dims))
+      return VAS_E_CUDA;
+    const int grid = sms;
+    const bool fp8 = d.kv_dtype == VAS_FP8_E4M3;
+    if (d.head_dim == 128 && d.page_size == 16)
+      return fp8 ? launch_bf16<128, 16, kKvFp8>(mk, mv, aa, grid, stream)
+                 : launch_bf16<128, 16, kKvInt8>(mk, mv, aa, grid, stream);
+    if (d.head_dim == 128)
+      return fp8 ? launch_bf16<128, 32, kKvFp8>(mk, mv, aa, grid, stream)
+                 : launch_bf16<128, 32, kKvInt8>(mk, mv, aa, grid, stream);
+    if (d.page_size == 16)
+      return fp8 ? launch_bf16<64, 16, kKvFp8>(mk, mv, aa, grid, stream)
+                 : launch_bf16<64, 16, kKvInt8>(mk, mv, aa, grid, stream);
+    return fp8 ? launch_bf16<64, 32, kKvFp8>(mk, mv, aa, grid, stream)
+               : launch_bf16<64, 32, kKvInt8>(mk, mv, aa, grid, stream);
+  }
   if (bf16) {
     CUtensorMap mk, mv;
     if (!encode_pool_map(&mk, k_pages, dims) || !encode_pool_map(&mv, v_pages, dims))
       return VAS_E_CUDA;
     const int grid = sms;
-    if (d.head_dim == 128 && d.page_size == 16) return launch_bf16<128, 16>(mk, mv, aa, grid, stream);
-    if (d.head_dim == 128) return launch_bf16<128, 32>(mk, mv, aa, grid, stream);
-    if (d.page_size == 16) return launch_bf16<64, 16>(mk, mv, aa, grid, stream);
-    return launch_bf16<64, 32>(mk, mv, aa, grid, stream);
+    if (d.head_dim == 128 && d.page_size == 16)
+      return launch_bf16<128, 16, kKvBf16>(mk, mv, aa, grid, stream);
+    if (d.head_dim == 128) return launch_bf16<128, 32, kKvBf16>(mk, mv, aa, grid, stream);
+    if (d.page_size == 16) return launch_bf16<64, 16, kKvBf16>(mk, mv, aa, grid, stream);
+    return launch_bf16<64, 32, kKvBf16>(mk, mv, aa, grid, stream);
   }
   const int grid = 4 * sms;
   if (d.head_dim == 128) attn_f32_kernel<128><<<grid, 128, 0, stream>>>(aa);
@@ -2163,8 +2495,8 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
                    const int32_t* query_lens, void* out, float* lse,
                    const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
                    vas_stream_t stream) {
-  return attn_launch(q, k_pages, v_pages, block_table, seq_lens, query_lens, nullptr, out, lse,
-                     dims, workspace, workspace_bytes, stream);
+  return attn_launch(q, k_pages, v_pages, nullptr, nullptr, block_table, seq_lens, query_lens,
+                     nullptr, out, lse, dims, workspace, workspace_bytes, stream);
 }
 
 int paged_attn_fwd_tree(const void* q, const void* k_pages, const void* v_pages,
@@ -2173,8 +2505,19 @@ int paged_attn_fwd_tree(const void* q, const void* k_pages, const void* v_pages,
                         float* lse, const vas_attn_dims* dims, void* workspace,
                         size_t workspace_bytes, vas_stream_t stream) {
   if (!tree_mask) return VAS_E_INVALID_ARG;
-  return attn_launch(q, k_pages, v_pages, block_table, seq_lens, query_lens, tree_mask, out, lse,
-                     dims, workspace, workspace_bytes, stream);
+  return attn_launch(q, k_pages, v_pages, nullptr, nullptr, block_table, seq_lens, query_lens,
+                     tree_mask, out, lse, dims, workspace, workspace_bytes, stream);
+}
+
+int paged_attn_fwd_quant(const void* q, const void* k_pages, const void* v_pages,
+                         const float* k_scale, const float* v_scale, const int32_t* block_table,
+                         const int32_t* seq_lens, const int32_t* query_lens,
+                         const uint64_t* tree_mask, void* out, float* lse,
+                         const vas_attn_dims* dims, void* workspace, size_t workspace_bytes,
+                         vas_stream_t stream) {
+  if (!dims || !kv_quantized(dims) || !k_scale || !v_scale) return VAS_E_INVALID_ARG;
+  return attn_launch(q, k_pages, v_pages, k_scale, v_scale, block_table, seq_lens, query_lens,
+                     tree_mask, out, lse, dims, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
