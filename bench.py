@@ -66,10 +66,13 @@ def measured_peak(key="hbm_gbs"):
 # Algorithmic bytes (each KV element read once per KV head, Q in, out + lse out, the
 # block-table entries used; spec_verify: the row(s) it must read plus scalars).
 # ---------------------------------------------------------------------------------
-def attn_bytes(seq_lens, query_lens, Hq, Hkv, D, P, elem):
+def attn_bytes(seq_lens, query_lens, Hq, Hkv, D, P, elem, kv_elem=None):
+    """elem: bytes of a q / out element; kv_elem: of a K/V element (default elem).  A
+    pool of 1-byte codes also reads one fp32 scale per token and KV head for K and V."""
     L = np.asarray(seq_lens, dtype=np.int64)
     ql = np.asarray(query_lens, dtype=np.int64)
-    kv = int((L * Hkv * D * 2 * elem).sum())
+    kv_elem = elem if kv_elem is None else kv_elem
+    kv = int((L * Hkv * (D * 2 * kv_elem + (8 if kv_elem == 1 else 0))).sum())
     qo = int((ql * Hq * D * 2 * elem).sum())
     bt = int(((L + P - 1) // P * 4).sum())
     lse = int((ql * Hq * 4).sum())
@@ -91,6 +94,14 @@ def verify_bytes(accepted_len, k, V):
     rows = np.where(acc < k, 2, 1)  # residual needs p_j and q_j; the bonus needs p_k
     scalars = k * 4 + k * 8 + (k + 1) * 4 + 4
     return int((rows * V * 4).sum() + len(acc) * scalars)
+
+
+def elem_sizes(kv_dtype):
+    """(bytes of a q / out element, bytes of a K/V element) of a storage type."""
+    from verify_attention_spec_gb300 import workloads as wl
+    if kv_dtype in wl.QUANTIZED:
+        return 2, 1
+    return (2, 2) if kv_dtype == wl.BF16 else (4, 4)
 
 
 def workload_desc(name):
@@ -208,18 +219,32 @@ def oracle_sample(a, seqs):
     for r, x in enumerate(nbt):
         btn[r, :len(x)] = x
     r = torch.from_numpy(np.concatenate(rows)).to(a.q.device)
+    if a.kv_dtype in wl.QUANTIZED:
+        np_ = lambda t: t.detach().cpu().contiguous().numpy()
+        return dict(q=wl.bf16_bits(a.q[r].cpu()), k=np_(a.k_pages[idx]), v=np_(a.v_pages[idx]),
+                    ks=np_(a.k_scale[idx]), vs=np_(a.v_scale[idx]), bt=btn, lens=lens[seqs],
+                    qlens=qlens[seqs])
     st = lambda t: wl.storage_for_oracle(t, a.kv_dtype)
     return dict(q=st(a.q[r]), k=st(a.k_pages[idx]), v=st(a.v_pages[idx]), bt=btn,
                 lens=lens[seqs], qlens=qlens[seqs])
 
 
-def time_oracle_attention(sample, kv_dtype):
+def run_oracle_attention(sample, kv_dtype):
     import oracle
     from verify_attention_spec_gb300 import workloads as wl
+    if kv_dtype in wl.QUANTIZED:
+        fmt = oracle.Q_E4M3 if kv_dtype == wl.FP8 else oracle.Q_INT8
+        return oracle.paged_attn_quant(sample["q"], sample["k"], sample["v"], sample["ks"],
+                                       sample["vs"], sample["bt"], sample["lens"], sample["qlens"],
+                                       fmt=fmt)
     code = oracle.BF16 if kv_dtype == wl.BF16 else oracle.F32
+    return oracle.paged_attn(sample["q"], sample["k"], sample["v"], sample["bt"], sample["lens"],
+                             sample["qlens"], dtype_code=code)
+
+
+def time_oracle_attention(sample, kv_dtype):
     t0 = time.perf_counter()
-    oracle.paged_attn(sample["q"], sample["k"], sample["v"], sample["bt"], sample["lens"],
-                      sample["qlens"], dtype_code=code)
+    run_oracle_attention(sample, kv_dtype)
     return time.perf_counter() - t0
 
 
@@ -248,7 +273,7 @@ def cpu_baseline(a, v, name):
             dt += time_oracle_attention(smp, a.kv_dtype)
         runs += extra
     by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
-                    w.page_size, 2 if w.kv_dtype == "bf16" else 4) * runs
+                    w.page_size, *elem_sizes(w.kv_dtype)) * runs
     out = {"value": by / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
            "sample": f"paged attention on {len(seqs)} of {a.num_seqs} sequences of {name}, "
                      f"{runs} run(s) ({by / 1e9:.3f} GB algorithmic, {dt:.1f} s)"}
@@ -323,16 +348,27 @@ def run_ours(args):
                                 pool_device=dev)
     else:
         a = wl.workload_attention(name, pool_device=dev)
-    a = wl.AttentionInputs(*(t.to(dev).contiguous() for t in (a.q, a.k_pages, a.v_pages,
-                                                               a.block_table, a.seq_lens,
-                                                               a.query_lens)),
-                           a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
+    mv = lambda t: None if t is None else t.to(dev).contiguous()
+    a = wl.AttentionInputs(*(mv(t) for t in (a.q, a.k_pages, a.v_pages, a.block_table,
+                                             a.seq_lens, a.query_lens)),
+                           a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype,
+                           mv(a.k_scale), mv(a.v_scale))
+    quant = a.kv_dtype if a.kv_dtype in wl.QUANTIZED else None
     v = wl.workload_verify(name)
     if args.max_seqs and v is not None:
         nv = max(1, int((qlens > 1).sum()))
         v = wl.VerifyInputs(v.p[:nv], v.q[:nv], v.draft[:nv], v.seed)
-    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
+    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens, quant=quant)
     ws = vas.alloc_workspace(dims, device=dev)
+
+    def attn(q_, bt_, sl_, ql_, out_, lse_):
+        """One attention call through the C ABI (quantised pools: paged_attn_fwd_quant)."""
+        if quant:
+            vas.paged_attn_fwd_quant(q_, a.k_pages, a.v_pages, a.k_scale, a.v_scale, bt_, sl_, ql_,
+                                     out_, lse_, ws, quant=quant, dims=dims)
+        else:
+            vas.paged_attn_fwd(q_, a.k_pages, a.v_pages, bt_, sl_, ql_, out_, lse_, ws, dims=dims)
+
     out = torch.empty_like(a.q)
     lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=dev)
     if v is not None:
@@ -343,14 +379,13 @@ def run_ours(args):
         tok_d = torch.empty(v.B, v.k + 1, dtype=torch.int32, device=dev)
 
     def step():
-        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
-                           out, lse, ws, dims=dims)
+        attn(a.q, a.block_table, a.seq_lens, a.query_lens, out, lse)
         if v is not None:
             vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
 
-    elem = 2 if a.kv_dtype == wl.BF16 else 4
+    elem, kv_elem = elem_sizes(a.kv_dtype)
     a_bytes = attn_bytes(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
-                         a.num_kv_heads, a.head_dim, a.page_size, elem)
+                         a.num_kv_heads, a.head_dim, a.page_size, elem, kv_elem)
     step()
     torch.cuda.synchronize()
     v_bytes = verify_bytes(acc_d.cpu().numpy(), v.k, v.V) if v is not None else 0
@@ -371,8 +406,7 @@ def run_ours(args):
     t_start.record()
     for i in range(K):
         ev[i][0].record()
-        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
-                           out, lse, ws, dims=dims)
+        attn(a.q, a.block_table, a.seq_lens, a.query_lens, out, lse)
         ev[i][1].record()
         if v is not None:
             vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
@@ -421,8 +455,7 @@ def run_ours(args):
             cs.wait_event(sl["up"])
             cs.wait_event(sl["down"])  # this slot's previous results have been read back
             q_, bt_, sl_, ql_ = sl["din"]
-            vas.paged_attn_fwd(q_, a.k_pages, a.v_pages, bt_, sl_, ql_, sl["dout"][0],
-                               sl["dout"][1], ws, dims=dims)
+            attn(q_, bt_, sl_, ql_, sl["dout"][0], sl["dout"][1])
             if v is not None:
                 vas.spec_verify(sl["dv"][0], sl["dv"][1], sl["dv"][2], v.seed, sl["dout"][2],
                                 sl["dout"][3])
@@ -486,12 +519,12 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if a.kv_dtype == wl.BF16 else "f32",
+        "dtype": a.kv_dtype,
         "data": "synthetic",
         "config": {"workload": workload_desc(name) + (f" (first {args.max_seqs} sequences only)"
                                                        if args.max_seqs else ""),
                    "l2": "inputs larger than L2 (KV pool %.1f GB per step)"
-                         % ((a.k_pages.numel() + a.v_pages.numel()) * elem / 1e9),
+                         % ((a.k_pages.numel() + a.v_pages.numel()) * kv_elem / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "paged_attn": {"gbs": attn_gbs, "ms": attn_ms, "algorithmic_bytes": a_bytes,
                        "algorithmic_flops": a_flops, "tflops": attn_tflops,
@@ -541,8 +574,8 @@ def run_reference(args):
     lens, qlens = wl.sample_lengths(w), wl.query_lengths(w)
     order = np.random.default_rng(0).permutation(len(lens))
     # a bounded sample: sequences in seeded order up to ~64 MB of KV
-    elem = 2 if w.kv_dtype == wl.BF16 else 4
-    per_tok = w.num_kv_heads * w.head_dim * 2 * elem
+    elem, kv_elem = elem_sizes(w.kv_dtype)
+    per_tok = w.num_kv_heads * w.head_dim * 2 * kv_elem
     seqs, tot = [], 0
     for i in order:
         if seqs and tot + lens[i] * per_tok > 64e6:
@@ -554,16 +587,12 @@ def run_reference(args):
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, kv_dtype=w.kv_dtype, seed=w.seed)
     v = wl.workload_verify(name)
-    code = oracle.BF16 if w.kv_dtype == wl.BF16 else oracle.F32
-    st = lambda t: wl.storage_for_oracle(t, w.kv_dtype)
-    smp = dict(q=st(a.q), k=st(a.k_pages), v=st(a.v_pages), bt=a.block_table.numpy(),
-               lens=a.seq_lens.numpy(), qlens=a.query_lens.numpy())
+    smp = oracle_sample(a, list(range(len(seqs))))
     by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
-                    w.page_size, elem)
+                    w.page_size, elem, kv_elem)
 
     def step():
-        oracle.paged_attn(smp["q"], smp["k"], smp["v"], smp["bt"], smp["lens"], smp["qlens"],
-                          dtype_code=code)
+        run_oracle_attention(smp, w.kv_dtype)
         if v is not None:
             oracle.spec_verify(v.p[:8], v.q[:8], v.draft[:8], v.seed)
 

@@ -26,3 +26,14 @@ def test_attn_bytes_counts_each_kv_element_once_per_kv_head():
     kv = 33 * 2 * 64 * 2 * 2
     qo = 2 * 8 * 64 * 2 * 2
     assert got == kv + qo + 3 * 4 + 2 * 8 * 4
+
+
+def test_attn_bytes_of_a_quantised_pool():
+    # 1-byte codes for K and V plus one fp32 scale per token and KV head for each; q and
+    # out stay bf16
+    got = bench.attn_bytes([33], [2], Hq=8, Hkv=2, D=64, P=16, elem=2, kv_elem=1)
+    kv = 33 * 2 * (64 * 2 * 1 + 2 * 4)
+    qo = 2 * 8 * 64 * 2 * 2
+    assert got == kv + qo + 3 * 4 + 2 * 8 * 4
+    from verify_attention_spec_gb300 import workloads as wl
+    assert bench.elem_sizes(wl.FP8) == (2, 1) and bench.elem_sizes(wl.BF16) == (2, 2)

@@ -63,15 +63,15 @@ constexpr int kProducerWarp = kConsumerWarps;      // TMA loads
 constexpr int kMmaWarp = kConsumerWarps + 1;       // tcgen05 issue for wide units
 constexpr int kThreads = kConsumerThreads + 64;    // + producer warp + MMA warp
 // Quantised KV pages (FP8 E4M3 or INT8 codes with fp32 scales per token and KV head):
-// the producer lands the codes and scales of a stage in a landing ring, and two
-// converter warps expand the codes into f16 stages of the same layout as bf16 stages.
-// Every product of such a call runs in f16 (codes exact; Q scaled into f16 range by a
-// power of two per unit; P in f16).
+// the producer lands a stage's codes in the upper half of its 16-bit slot and its
+// scales beside the ring; a converter warp expands the codes in place into f16 in the
+// bf16 stage layout and marks the stage ready.  Every product of such a call runs in
+// f16 (codes exact; Q scaled into f16 range by a power of two per unit; P in f16, whose
+// 11 bits make the two-part P of precise row blocks unnecessary).
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvInt8 = 2;
 constexpr int kConvWarps = 2;
 constexpr int kConvWarp0 = kMmaWarp + 1;
 constexpr int kThreadsQ = kThreads + 32 * kConvWarps;
-constexpr int kLandSlots = 6;  // a multiple of kConvWarps (each converter keeps its slots)
 constexpr int kTmemCols = 256;
 constexpr int kTmemS = 0;    // S of a prompt-chunk stage, two 32-column buffers
 constexpr int kTmemO = 64;   // O: 128 lanes x D fp32
@@ -82,7 +82,6 @@ constexpr int kRowBlockTc = 128;   // ... or, for sequences with more rows (prom
 __host__ __device__ __forceinline__ int row_block(int R) {
   return R > kRowBlock ? kRowBlockTc : kRowBlock;
 }
-static_assert(kLandSlots % kConvWarps == 0, "landing slots must be a multiple of the converters");
 constexpr int kNarrowRows = 16;    // units with at most this many rows take the K Q^T form
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
@@ -439,10 +438,11 @@ struct Smem {
   // s % kConsumerWarps == w and waits on slot s % kSlots by phase parity.  The parity
   // test is only sound if the slot's previous fill was consumed by the same warp, i.e.
   // if kSlots is a multiple of the number of consumer warps; otherwise a warp could pass
-  // the parity test while the slot's previous fill is still in flight.  Quantised pools
-  // keep fewer 16-bit stages: their landing ring holds the stages in flight.
-  static constexpr int kSlots = KQ == kKvBf16 ? 8 : 4;
-  static_assert(kSlots % kConsumerWarps == 0, "stage slots must be a multiple of the consumer warps");
+  // the parity test while the slot's previous fill is still in flight.  The same holds
+  // for the converters of quantised pools (stage s goes to converter s % kConvWarps).
+  static constexpr int kSlots = 8;
+  static_assert(kSlots % kConsumerWarps == 0 && kSlots % kConvWarps == 0,
+                "stage slots must be a multiple of the consumer warps and of the converters");
   static constexpr int NH = D / 64;                        // 128-byte halves per token row
   static constexpr int kRowBytes = D * 2;
   static constexpr int kOperandBytes = kStageTokens * kRowBytes;  // K or V of one stage
@@ -461,34 +461,34 @@ struct Smem {
   // Prompt-chunk units: their query tile (128 rows, K-major 128-byte swizzle,
   // [D/64][row][64]) after the P tiles.
   static constexpr int kQTileOff = kPTileOff + 2 * kPTileBytes;
-  // Precise units: the rounding error of each P tile as a second bf16 tile.
+  // Precise units: the rounding error of each P tile as a second bf16 tile (bf16 calls
+  // only).
   static constexpr int kPLoOff = kQTileOff + 128 * D * 2;
-  static constexpr int kWideBytes = kPLoOff + 2 * kPTileBytes;
+  static constexpr int kWideBytes = kPLoOff + (KQ == kKvBf16 ? 2 * kPTileBytes : 0);
   static constexpr int kMergeBytes = kNarrowBytes > kWideBytes ? kNarrowBytes : kWideBytes;
   static constexpr int kScratchBytes = kQBytes > kMergeBytes ? kQBytes : kMergeBytes;
   static constexpr int kScratchOff = kSlots * kStageBytes;
   static constexpr int kRingOff = kScratchOff + ((kScratchBytes + 127) / 128) * 128;
-  // Quantised pools: the landing ring (per slot the stage's K codes [32][D] bytes, V
-  // codes, 32 K scales, 32 V scales) and the scales of each 16-bit stage (32 K, 32 V).
-  static constexpr int kNLand = KQ == kKvBf16 ? 0 : kLandSlots;
-  static constexpr int kLandCodes = kStageTokens * D;
-  static constexpr int kLandStride = ((2 * kLandCodes + 2 * kStageTokens * 4 + 127) / 128) * 128;
-  static constexpr int kLandOff = kRingOff + kRing * (int)sizeof(RingEntry);
-  static constexpr int kScaleOff = kLandOff + kNLand * kLandStride;
-  static constexpr int kBarOff = kScaleOff + (kNLand ? kSlots * 2 * kStageTokens * 4 : 0);
+  // Quantised pools: a stage's codes land in the upper half of its slot, K codes
+  // [32][D] bytes at kCodeOff, V codes after them; its scales (32 K, 32 V) in the
+  // scale array.
+  static constexpr bool kQ = KQ != kKvBf16;
+  static constexpr int kCodeOff = kOperandBytes;
+  static constexpr int kScaleOff = kRingOff + kRing * (int)sizeof(RingEntry);
+  static constexpr int kBarOff = kScaleOff + (kQ ? kSlots * 2 * kStageTokens * 4 : 0);
   // full[kSlots], empty[kSlots], ufull[kRing], uempty[kRing], tensor-memory unit
-  // barriers bp[2], bo[2], bs[2], bq, bfin, landing lfull[kNLand], lempty[kNLand] |
-  // meta[kSlots], flag[4], tmem base, qmax[4], lmeta[kNLand]
+  // barriers bp[2], bo[2], bs[2], bq, bfin, ready[kSlots] (quantised pools) |
+  // meta[kSlots], flag[4], tmem base, qmax[4]
   static constexpr int kWideBars = 8;
-  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars + 2 * kNLand) * 8 +
-                                   (kSlots + 4 + 1 + 4 + kNLand) * 4;
+  static constexpr int kBarBytes = (2 * kSlots + 2 * kRing + kWideBars + (kQ ? kSlots : 0)) * 8 +
+                                   (kSlots + 4 + 1 + 4) * 4;
   // Draft-tree masks of the unit's rows (row r: its token's mask, own bit set).
   static constexpr int kTmaskOff = ((kBarOff + kBarBytes + 7) / 8) * 8;
   static constexpr int kBytes = kTmaskOff + kRowBlockTc * 8;
   static constexpr int kDynBytes = kBytes + 1024;  // slack for 1024-byte alignment
   static_assert(kDynBytes <= 227 * 1024, "shared memory of one CTA");
   static_assert(kPLoOff % 1024 == 0 && kQTileOff % 1024 == 0, "swizzle atoms of the tiles");
-  static_assert(kLandOff % 128 == 0 && kLandStride % 128 == 0, "landing slots");
+  static_assert(kScaleOff % 16 == 0, "scale arrays take bulk copies");
 };
 
 // Byte offset of 16-byte column chunk gc of token row t inside one operand of a stage.
@@ -1026,15 +1026,15 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
   uint64_t* bs = bo + 2;
   uint64_t* bq = bs + 2;
   uint64_t* bfin = bq + 1;
-  uint64_t* lfull = bfin + 1;  // landing ring (quantised pools)
-  uint64_t* lempty = lfull + S::kNLand;
-  int32_t* meta = reinterpret_cast<int32_t*>(lempty + S::kNLand);
+  uint64_t* ready = bfin + 1;  // quantised pools: the stage's codes are converted
+  int32_t* meta = reinterpret_cast<int32_t*>(ready + (kQuant ? kSlots : 0));
   int32_t* flag = meta + kSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(flag + 4);
   float* qmax = reinterpret_cast<float*>(tmem_slot + 1);
-  int32_t* lmeta = reinterpret_cast<int32_t*>(qmax + 4);
-  uint8_t* land = smem + S::kLandOff;
   float* stage_scales = reinterpret_cast<float*>(smem + S::kScaleOff);  // [kSlots][K 32 | V 32]
+  // What the consumers and the MMA warp wait on before reading a stage: its copies
+  // (bf16), or its conversion (quantised pools; the converter waits on the copies).
+  uint64_t* stage_ready = kQuant ? ready : full;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -1047,10 +1047,8 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
       // consumers, the MMA warp and (quantised pools) the converters
       mbar_init(&uempty[r], kConsumerWarps + 1 + (kQuant ? kConvWarps : 0));
     }
-    for (int s = 0; s < S::kNLand; ++s) {
-      mbar_init(&lfull[s], 1);
-      mbar_init(&lempty[s], 1);
-    }
+    if (kQuant)
+      for (int s = 0; s < kSlots; ++s) mbar_init(&ready[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bp[b], kConsumerWarps);
       mbar_init(&bo[b], 1);
@@ -1142,11 +1140,8 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
           const int32_t my_id =
               pg0 == it.page_begin ? bt_cur : (lane < npg ? bt_row[pg0 + lane] : 0);
           for (int s0 = 0; s0 < npg; s0 += PPS) {
-            // bf16: the stage goes to 16-bit slot stage % kSlots; quantised: to landing
-            // slot stage % kLandSlots, which a converter empties.
-            const int slot_s = kQuant ? stage_it % kLandSlots : stage_it % kSlots;
-            ok = kQuant ? mbar_wait(&lempty[slot_s], ((stage_it / kLandSlots) & 1) ^ 1)
-                        : mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1);
+            const int slot_s = stage_it % kSlots;
+            ok = mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1);
             if (!ok) break;
             const int n_in = min(PPS, npg - s0);
             int ids[PPS];
@@ -1161,22 +1156,23 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
               }
             }
             if (kQuant && lane == 0) {
-              // Codes: one box per page and operand, [P tokens][D bytes]; scales: P
-              // floats per page, head and operand, contiguous in [page][head][slot].
-              lmeta[slot_s] = bad;
-              mbar_arrive_expect_tx(&lfull[slot_s], bytes);
-              uint8_t* kdst = land + slot_s * S::kLandStride;
-              uint8_t* vdst = kdst + S::kLandCodes;
-              float* ksd = reinterpret_cast<float*>(vdst + S::kLandCodes);
+              // Codes: one box per page and operand, [P tokens][D bytes], into the upper
+              // half of the slot (K codes, then V codes); scales: P floats per page, head
+              // and operand, contiguous in [page][head][slot].
+              meta[slot_s] = bad;
+              mbar_arrive_expect_tx(&full[slot_s], bytes);
+              uint8_t* kdst = stages + slot_s * S::kStageBytes + S::kCodeOff;
+              uint8_t* vdst = kdst + kStageTokens * D;
+              float* ksd = stage_scales + slot_s * 2 * kStageTokens;
               float* vsd = ksd + kStageTokens;
 #pragma unroll
               for (int e = 0; e < PPS; ++e) {
                 if (e < n_in && ids[e] >= 0 && ids[e] < a.num_pages) {
-                  tma_load_3d(kdst + e * P * D, &tm_k, &lfull[slot_s], 0, ids[e] * P, head, pol);
-                  tma_load_3d(vdst + e * P * D, &tm_v, &lfull[slot_s], 0, ids[e] * P, head, pol);
+                  tma_load_3d(kdst + e * P * D, &tm_k, &full[slot_s], 0, ids[e] * P, head, pol);
+                  tma_load_3d(vdst + e * P * D, &tm_v, &full[slot_s], 0, ids[e] * P, head, pol);
                   const size_t so = ((size_t)ids[e] * a.Hkv + head) * P;
-                  bulk_load(ksd + e * P, a.k_scale + so, P * 4, &lfull[slot_s], pol);
-                  bulk_load(vsd + e * P, a.v_scale + so, P * 4, &lfull[slot_s], pol);
+                  bulk_load(ksd + e * P, a.k_scale + so, P * 4, &full[slot_s], pol);
+                  bulk_load(vsd + e * P, a.v_scale + so, P * 4, &full[slot_s], pol);
                 }
               }
             }
@@ -1212,25 +1208,24 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
     if (!ok && lane == 0) atomicOr(a.err, VAS_DEV_TIMEOUT);
     pdl_launch_dependents();  // no more work for this CTA: the next kernel may launch
     // Let every copy this warp issued land before the CTA can exit.
-    if constexpr (kQuant) {
-      for (uint32_t d = stage_it > kLandSlots ? stage_it - kLandSlots : 0; d < stage_it; ++d)
-        mbar_wait(&lfull[d % kLandSlots], (d / kLandSlots) & 1);
-    } else {
-      for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
-        mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
-    }
+    for (uint32_t d = stage_it > kSlots ? stage_it - kSlots : 0; d < stage_it; ++d)
+      mbar_wait(&full[d % kSlots], (d / kSlots) & 1);
     return;
   }
 
   if (kQuant && warp >= kConvWarp0) {
     // ------------------------------ converters ------------------------------
     // Follow the unit ring.  Converter c takes the stages s with s % kConvWarps == c:
-    // it waits for landing slot s % kLandSlots and for 16-bit slot s % kSlots to be
-    // free, expands the codes to f16 in the bf16 stage layout, copies the stage's
-    // scales (zero past the loaded tokens and past the sequence end, where the pool
-    // may hold anything), and arrives on the stage's full barrier.  Both ring sizes are
-    // multiples of kConvWarps, so each converter waits only on slots it used last.
+    // once the stage's copies have landed (full) it expands the codes in place -- K codes
+    // from the upper half of the slot into the K operand, then V codes, all read before
+    // any is overwritten, into the V operand -- zeroes the scales past the loaded tokens
+    // and past the sequence end (the pool may hold anything there), and marks the stage
+    // ready.  kSlots is a multiple of kConvWarps, so each converter waits only on slots
+    // it handled last.
     const int cw = warp - kConvWarp0;
+    constexpr int kC = D / 16;                           // 16-code chunks per token row
+    constexpr int kPer = kStageTokens * kC / 32;  // chunks per lane per operand
+    static_assert(32 % kC == 0, "a lane keeps one code chunk of its token rows");
     uint32_t stage_it = 0, unit_it = 0;
     bool ok = true;
     for (;;) {
@@ -1250,56 +1245,81 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
       const int n_stages = (it.page_end - it.page_begin + PPS - 1) / PPS;
       for (int si = 0; si < n_stages; ++si, ++stage_it) {
         if ((int)(stage_it % kConvWarps) != cw) continue;
-        const int ls = stage_it % kLandSlots, slot_s = stage_it % kSlots;
-        if (!mbar_wait(&lfull[ls], (stage_it / kLandSlots) & 1) ||
-            !mbar_wait(&empty[slot_s], ((stage_it / kSlots) & 1) ^ 1)) {
+        const int slot_s = stage_it % kSlots;
+        if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
           ok = false;
           break;
         }
         const int pg = it.page_begin + si * PPS;
         const int loaded = min(PPS, it.page_end - pg) * P;
         const int t_abs0 = pg * P;
-        const uint8_t* lk = land + ls * S::kLandStride;
-        const uint8_t* lv = lk + S::kLandCodes;
-        const float* lks = reinterpret_cast<const float*>(lv + S::kLandCodes);
         uint8_t* kt = stages + slot_s * S::kStageBytes;
         uint8_t* vt = kt + S::kOperandBytes;
-        constexpr int kC = D / 16;  // 16-code chunks per token row
-        for (int c = lane; c < loaded * kC; c += 32) {
-          const int t = c / kC, ch = c % kC;
+        const uint8_t* kc = kt + S::kCodeOff;
+        const uint8_t* vc = kc + kStageTokens * D;
+        auto expand = [&](uint4 x, uint4& y0, uint4& y1) {
+          if constexpr (KQ == kKvFp8) {
+            e4m3x4_to_f16x4(x.x, y0.x, y0.y);
+            e4m3x4_to_f16x4(x.y, y0.z, y0.w);
+            e4m3x4_to_f16x4(x.z, y1.x, y1.y);
+            e4m3x4_to_f16x4(x.w, y1.z, y1.w);
+          } else {
+            s8x4_to_f16x4(x.x, y0.x, y0.y);
+            s8x4_to_f16x4(x.y, y0.z, y0.w);
+            s8x4_to_f16x4(x.z, y1.x, y1.y);
+            s8x4_to_f16x4(x.w, y1.z, y1.w);
+          }
+        };
+        // Chunk i of this lane: token t0 + (32 / kC) i, code chunk ch (fixed per lane),
+        // so every offset below is a per-lane constant plus an immediate.
+        const int t0 = lane / kC, ch = lane % kC;
+        // K: its codes lie above the K operand, so each chunk goes straight out.
+        uint4 xk[kPer];
 #pragma unroll
-          for (int op = 0; op < 2; ++op) {
-            const uint4 x = *reinterpret_cast<const uint4*>((op ? lv : lk) + t * D + ch * 16);
+        for (int i = 0; i < kPer; ++i) {
+          const int t = t0 + (32 / kC) * i;
+          xk[i] = t < loaded ? *reinterpret_cast<const uint4*>(kc + t * D + ch * 16)
+                             : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int t = t0 + (32 / kC) * i;
+          if (t < loaded) {
             uint4 y0, y1;
-            if constexpr (KQ == kKvFp8) {
-              e4m3x4_to_f16x4(x.x, y0.x, y0.y);
-              e4m3x4_to_f16x4(x.y, y0.z, y0.w);
-              e4m3x4_to_f16x4(x.z, y1.x, y1.y);
-              e4m3x4_to_f16x4(x.w, y1.z, y1.w);
-            } else {
-              s8x4_to_f16x4(x.x, y0.x, y0.y);
-              s8x4_to_f16x4(x.y, y0.z, y0.w);
-              s8x4_to_f16x4(x.z, y1.x, y1.y);
-              s8x4_to_f16x4(x.w, y1.z, y1.w);
-            }
-            uint8_t* dst = op ? vt : kt;
-            *reinterpret_cast<uint4*>(dst + kv_off<D, P>(t, 2 * ch)) = y0;
-            *reinterpret_cast<uint4*>(dst + kv_off<D, P>(t, 2 * ch + 1)) = y1;
+            expand(xk[i], y0, y1);
+            *reinterpret_cast<uint4*>(kt + kv_off<D, P>(t, 2 * ch)) = y0;
+            *reinterpret_cast<uint4*>(kt + kv_off<D, P>(t, 2 * ch + 1)) = y1;
+          }
+        }
+        // V: its f16 rows cover the K and V codes; read them all first.
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int t = t0 + (32 / kC) * i;
+          xk[i] = t < loaded ? *reinterpret_cast<const uint4*>(vc + t * D + ch * 16)
+                             : make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int t = t0 + (32 / kC) * i;
+          if (t < loaded) {
+            uint4 y0, y1;
+            expand(xk[i], y0, y1);
+            *reinterpret_cast<uint4*>(vt + kv_off<D, P>(t, 2 * ch)) = y0;
+            *reinterpret_cast<uint4*>(vt + kv_off<D, P>(t, 2 * ch + 1)) = y1;
           }
         }
         {
           const bool live = lane < loaded && t_abs0 + lane < L;
           float* sc = stage_scales + slot_s * 2 * kStageTokens;
-          sc[lane] = live ? lks[lane] : 0.f;
-          sc[kStageTokens + lane] = live ? lks[kStageTokens + lane] : 0.f;
+          if (!live) {
+            sc[lane] = 0.f;
+            sc[kStageTokens + lane] = 0.f;
+          }
         }
-        if (lane == 0) meta[slot_s] = lmeta[ls];
         fence_proxy_async_smem();  // tcgen05 reads these stages as operands
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&lempty[ls]);
-          mbar_arrive(&full[slot_s]);
-        }
+        if (lane == 0) mbar_arrive(&ready[slot_s]);
       }
       if (!ok) break;
     }
@@ -1364,7 +1384,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         auto issue_s = [&](int j) -> bool {
           const uint32_t st = stage_it + j;
           const int slot_s = st % kSlots;
-          if (!mbar_wait(&full[slot_s], (st / kSlots) & 1)) return false;
+          if (!mbar_wait(&stage_ready[slot_s], (st / kSlots) & 1)) return false;
           if (lane == 0) {
             tc_fence_after();
             const uint32_t k_lo = umma_desc_lo(smem_u32(stages + slot_s * S::kStageBytes), 16);
@@ -1419,7 +1439,8 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
           }
           return good;
         };
-        ok = precise ? stages_pv(std::true_type{}) : stages_pv(std::false_type{});
+        if constexpr (kQuant) ok = stages_pv(std::false_type{});  // f16 P needs no low part
+        else ok = precise ? stages_pv(std::true_type{}) : stages_pv(std::false_type{});
         wk += n_stages;
         wc += n_stages;
         stage_it += n_stages;
@@ -1609,7 +1630,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         // S of this stage is in TMEM; its commit also covers the product that last read
         // P tile b.
         const bool got = mbar_wait_fast(&bs[kc & 1], (kc >> 1) & 1) &&
-                         mbar_wait_fast(&full[slot_s], (stage_it / kSlots) & 1);
+                         mbar_wait_fast(&stage_ready[slot_s], (stage_it / kSlots) & 1);
         if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
           timed_out = true;
           stage_it += n_stages - si;
@@ -1683,8 +1704,11 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
           }
           const float mu = mref == -INFINITY ? 0.f : mref;
           uint8_t* prow = scratch + S::kPTileOff + b * S::kPTileBytes + r * 128;
-          l += precise ? chunk_p_row<D, true, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens)
-                       : chunk_p_row<D, false, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens);
+          if constexpr (kQuant)  // f16 P needs no low part
+            l += chunk_p_row<D, false, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens);
+          else
+            l += precise ? chunk_p_row<D, true, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens)
+                         : chunk_p_row<D, false, KQ>(sr, valid, c, mu, prow, r, kss + kStageTokens);
           fence_proxy_async_smem();
         }
         tc_fence_before();
@@ -1778,7 +1802,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         for (int si = 0; si < n_stages; ++si, ++stage_it) {
           if ((int)(stage_it % kConsumerWarps) != warp) continue;
           const int slot_s = stage_it % kSlots;
-          if (!mbar_wait(&full[slot_s], (stage_it / kSlots) & 1)) {
+          if (!mbar_wait(&stage_ready[slot_s], (stage_it / kSlots) & 1)) {
             timed_out = true;
             stage_it += n_stages - si;
             break;
@@ -1927,7 +1951,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         for (int h = 0; h < nst; ++h) {
           const uint32_t st = stage_it + h;
           const int slot_s = st % kSlots;
-          got = got && mbar_wait_fast(&full[slot_s], (st / kSlots) & 1);
+          got = got && mbar_wait_fast(&stage_ready[slot_s], (st / kSlots) & 1);
           if (meta[slot_s]) poison = true;
           const int pg = it.page_begin + (2 * sj + h) * PPS;
           const int ld = min(PPS, it.page_end - pg) * P;
