@@ -79,6 +79,20 @@ def attn_bytes(seq_lens, query_lens, Hq, Hkv, D, P, elem, kv_elem=None):
     return kv + qo + bt + lse
 
 
+def unique_kv_bytes(block_table, seq_lens, Hkv, D, P, kv_elem):
+    """KV bytes of the distinct pages the batch reads (pages shared by several block
+    tables counted once, each with the most slots any of them uses)."""
+    bt = np.asarray(block_table)
+    L = np.asarray(seq_lens, dtype=np.int64)
+    used = {}
+    for i, l in enumerate(L):
+        for j in range(int((l + P - 1) // P)):
+            pg = int(bt[i, j])
+            used[pg] = max(used.get(pg, 0), int(min(P, l - j * P)))
+    per_tok = Hkv * (D * 2 * kv_elem + (8 if kv_elem == 1 else 0))
+    return int(sum(used.values())) * per_tok
+
+
 def attn_flops(seq_lens, query_lens, Hq, D):
     """Algorithmic flops: query row (token j, head h) of sequence i attends positions
     0 .. L_i - ql_i + j, two products of 2 D flops per position."""
@@ -386,6 +400,14 @@ def run_ours(args):
     elem, kv_elem = elem_sizes(a.kv_dtype)
     a_bytes = attn_bytes(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
                          a.num_kv_heads, a.head_dim, a.page_size, elem, kv_elem)
+    # Prefix sharing: the KV bytes of distinct pages (what HBM must deliver at least)
+    # against the per-sequence count in a_bytes.
+    kv_logical = attn_bytes(a.seq_lens.cpu().numpy(), np.zeros(a.num_seqs), 0, a.num_kv_heads,
+                            a.head_dim, a.page_size, elem, kv_elem) - \
+        int(((a.seq_lens.cpu().numpy().astype(np.int64) + a.page_size - 1) // a.page_size * 4).sum())
+    kv_unique = unique_kv_bytes(a.block_table.cpu().numpy(), a.seq_lens.cpu().numpy(),
+                                a.num_kv_heads, a.head_dim, a.page_size, kv_elem)
+    a_bytes_unique = a_bytes - kv_logical + kv_unique
     step()
     torch.cuda.synchronize()
     v_bytes = verify_bytes(acc_d.cpu().numpy(), v.k, v.V) if v is not None else 0
@@ -527,6 +549,8 @@ def run_ours(args):
                          % ((a.k_pages.numel() + a.v_pages.numel()) * kv_elem / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "paged_attn": {"gbs": attn_gbs, "ms": attn_ms, "algorithmic_bytes": a_bytes,
+                       "distinct_page_bytes": a_bytes_unique,
+                       "distinct_page_gbs": a_bytes_unique / (attn_ms * 1e-3) / 1e9,
                        "algorithmic_flops": a_flops, "tflops": attn_tflops,
                        "frac_of_measured_peak": attn_gbs / peak,
                        "frac_of_nominal_8tbs": attn_gbs / NOMINAL_HBM_GBS},

@@ -37,3 +37,14 @@ def test_attn_bytes_of_a_quantised_pool():
     assert got == kv + qo + 3 * 4 + 2 * 8 * 4
     from verify_attention_spec_gb300 import workloads as wl
     assert bench.elem_sizes(wl.FP8) == (2, 1) and bench.elem_sizes(wl.BF16) == (2, 2)
+
+
+def test_unique_kv_bytes_counts_shared_pages_once():
+    # two sequences sharing pages 5 and 6 (32 tokens) and each with a page of its own
+    bt = np.array([[5, 6, 1], [5, 6, 2]])
+    got = bench.unique_kv_bytes(bt, [40, 35], Hkv=2, D=8, P=16, kv_elem=2)
+    tokens = 16 + 16 + 8 + 3
+    assert got == tokens * 2 * 8 * 2 * 2
+    # without sharing it equals the per-sequence count
+    bt2 = np.array([[5, 6, 1], [7, 8, 2]])
+    assert bench.unique_kv_bytes(bt2, [40, 35], 2, 8, 16, 2) == (40 + 35) * 2 * 8 * 2 * 2

@@ -195,3 +195,19 @@ def test_prefill8_sampled(vas_lib):
         compare_attention(out, lse, ref_o, ref_l, wl.BF16, rows=rows)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     assert vas_lib.vas_last_device_error() == 0
+
+
+def test_shared_prefix_pages(vas_lib):
+    """Block tables that alias a prefix: groups of 3 sequences share their first 4 pages
+    (a 64-token prompt), in decode, verify and chunk form, against the oracle."""
+    lens = np.array([70, 64 + 33, 64 + 200, 64 + 5, 64 + 1000, 90, 64 + 17])
+    qlens = np.array([1, 5, 33, 1, 9, 1, 2])
+    a = wl.attention_inputs(lens, qlens, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                            page_size=16, kv_dtype=wl.BF16, seed=23, prefix_pages=4,
+                            prefix_group=3)
+    bt = a.block_table.numpy()
+    assert (bt[0, :4] == bt[2, :4]).all() and (bt[3, :4] == bt[5, :4]).all()
+    ref_o, ref_l = oracle_attention(a)
+    out, lse = run_gpu_attention(vas_lib, to_device(a))
+    compare_attention(out, lse, ref_o, ref_l, wl.BF16)
+    assert vas_lib.vas_last_device_error() == 0

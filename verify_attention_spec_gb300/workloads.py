@@ -30,6 +30,9 @@ and beyond them, for chunked prefill:
                   (query length 1024, causal within the chunk), 70B attention shape,
                   bf16, page 32; no spec_verify;
 
+for prefix sharing, ``shared70b``: the 70B batch with a 2048-token system prompt in
+front of every sequence, its 64 pages shared by groups of 8 consecutive sequences;
+
 and for quantised KV pages, the 70B batch and decode64 with the same lengths, seeds and
 spec_verify, their K/V stored as FP8 E4M3 or INT8 codes with one fp32 scale per
 (token, KV head) for K and one for V (``stress70b_fp8``, ``stress70b_int8``,
@@ -80,6 +83,8 @@ class Workload:
     pool_pages: Optional[int] = None     # None: sized for the total
     fixed_lens: Optional[tuple] = None
     fixed_qlens: Optional[tuple] = None
+    prefix_tokens: int = 0     # a shared prefix (whole pages) added to every sequence ...
+    prefix_group: int = 0      # ... shared by consecutive groups of this many sequences
 
 
 WORKLOADS = {
@@ -97,6 +102,11 @@ WORKLOADS = {
     "prefill8": Workload("prefill8", 7, 64, 8, 128, 32, BF16, "fixed", (), 8, 0, 0, 0,
                          fixed_lens=(4096,) * 8, fixed_qlens=(1024,) * 8),
 }
+# Prefix sharing: the 70B batch with a 2048-token system prompt in front of every
+# sequence, shared by groups of 8 consecutive sequences (their block tables point at
+# the same 64 prompt pages).
+WORKLOADS["shared70b"] = dataclasses.replace(WORKLOADS["stress70b"], name="shared70b",
+                                             prefix_tokens=2048, prefix_group=8)
 for _base in ("stress70b", "decode64"):
     for _q in QUANTIZED:
         WORKLOADS[f"{_base}_{_q}"] = dataclasses.replace(WORKLOADS[_base], name=f"{_base}_{_q}",
@@ -142,9 +152,14 @@ def query_lengths(w: Workload) -> np.ndarray:
     return ql
 
 
-def build_pool(lens: np.ndarray, page_size: int, seed: int, pool_pages: Optional[int] = None):
+def build_pool(lens: np.ndarray, page_size: int, seed: int, pool_pages: Optional[int] = None,
+               prefix_pages: int = 0, prefix_group: int = 0):
     """Block table [B, max_pages] (padded with -1) over a seeded random permutation of
-    the pool.  Returns (block_table int32, num_pages)."""
+    the pool.  With prefix_pages, consecutive groups of prefix_group sequences share
+    their first prefix_pages pages (one copy per group).  Returns (block_table int32,
+    num_pages)."""
+    if prefix_pages:
+        return _build_shared_pool(lens, page_size, seed, prefix_pages, prefix_group)
     npages = (lens + page_size - 1) // page_size
     total = int(npages.sum())
     num_pages = total if pool_pages is None else int(pool_pages)
@@ -158,6 +173,26 @@ def build_pool(lens: np.ndarray, page_size: int, seed: int, pool_pages: Optional
         bt[i, :n] = perm[off:off + n]
         off += n
     return bt, num_pages
+
+
+def _build_shared_pool(lens, page_size, seed, prefix_pages, group):
+    npages = (lens + page_size - 1) // page_size
+    if np.any(npages <= prefix_pages):
+        raise ValueError("every sequence must extend past the shared prefix")
+    groups = (len(lens) + group - 1) // group
+    total = groups * prefix_pages + int((npages - prefix_pages).sum())
+    perm = _rng(seed, 3).permutation(total)
+    bt = np.full((len(lens), int(npages.max())), -1, dtype=np.int32)
+    off = 0
+    for gi in range(groups):
+        shared = perm[off:off + prefix_pages]
+        off += prefix_pages
+        for i in range(gi * group, min(len(lens), (gi + 1) * group)):
+            bt[i, :prefix_pages] = shared
+            n = int(npages[i]) - prefix_pages
+            bt[i, prefix_pages:prefix_pages + n] = perm[off:off + n]
+            off += n
+    return bt, total
 
 
 def _torch_dtype(kv_dtype: str):
@@ -231,12 +266,13 @@ class AttentionInputs:
 
 
 def attention_inputs(lens, qlens, *, num_q_heads, num_kv_heads, head_dim, page_size, kv_dtype,
-                     seed, pool_pages=None, pool_device="cpu") -> AttentionInputs:
+                     seed, pool_pages=None, pool_device="cpu", prefix_pages=0,
+                     prefix_group=0) -> AttentionInputs:
     """Paged attention inputs for explicit lengths.  The page pool (every slot, used or
     not) holds N(0,1) values drawn on `pool_device`; Q is drawn on the CPU."""
     lens = np.asarray(lens, dtype=np.int64)
     qlens = np.asarray(qlens, dtype=np.int64)
-    bt, num_pages = build_pool(lens, page_size, seed, pool_pages)
+    bt, num_pages = build_pool(lens, page_size, seed, pool_pages, prefix_pages, prefix_group)
     dt = _torch_dtype(kv_dtype)
     shape = (num_pages, page_size, num_kv_heads, head_dim)
     k_scale = v_scale = None
@@ -262,7 +298,7 @@ def draft_tree_parents(qlens, seed: int, extra_roots: float = 0.0) -> np.ndarray
     (the last accepted token); token j > 0 hangs under a uniformly drawn earlier token (a
     random recursive tree: bushy near the root, as top-k drafting makes it), or becomes a
     root of its own with probability `extra_roots` (a forest)."""
-    rng = _rng(seed, 3)
+    rng = _rng(seed, 5)
     out = []
     for ql in np.asarray(qlens, dtype=np.int64):
         par = np.full(int(ql), -1, dtype=np.int32)
@@ -274,10 +310,12 @@ def draft_tree_parents(qlens, seed: int, extra_roots: float = 0.0) -> np.ndarray
 
 def workload_attention(name: str, pool_device="cpu") -> AttentionInputs:
     w = WORKLOADS[name]
-    return attention_inputs(sample_lengths(w), query_lengths(w), num_q_heads=w.num_q_heads,
-                            num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                            page_size=w.page_size, kv_dtype=w.kv_dtype, seed=w.seed,
-                            pool_pages=w.pool_pages, pool_device=pool_device)
+    return attention_inputs(sample_lengths(w) + w.prefix_tokens, query_lengths(w),
+                            num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                            head_dim=w.head_dim, page_size=w.page_size, kv_dtype=w.kv_dtype,
+                            seed=w.seed, pool_pages=w.pool_pages, pool_device=pool_device,
+                            prefix_pages=w.prefix_tokens // w.page_size,
+                            prefix_group=w.prefix_group)
 
 
 @dataclasses.dataclass
