@@ -73,6 +73,11 @@ def _load():
     lib.oracle_spec_verify_given_uniforms.restype = i32
     lib.oracle_spec_verify.argtypes = [P, P, P, u64, i32, i32, i32, dbl, P, P, P, P, P]
     lib.oracle_spec_verify.restype = i32
+    lib.oracle_spec_verify_tree_given_uniforms.argtypes = [P, P, P, P, P, P, i32, i32, i32, dbl,
+                                                           P, P, P, P, P, P]
+    lib.oracle_spec_verify_tree_given_uniforms.restype = i32
+    lib.oracle_spec_verify_tree.argtypes = [P, P, P, P, u64, i32, i32, i32, dbl, P, P, P, P, P, P]
+    lib.oracle_spec_verify_tree.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
     _lib = lib
@@ -183,13 +188,14 @@ def uniforms(seed: int, B: int, k: int):
 
 
 class VerifyResult:
-    def __init__(self, accepted_len, out_tokens, margin, flag_pos, fallback, status):
+    def __init__(self, accepted_len, out_tokens, margin, flag_pos, fallback, status, path=None):
         self.accepted_len = accepted_len
         self.out_tokens = out_tokens
         self.margin = margin
         self.flag_pos = flag_pos
         self.fallback = fallback
         self.status = status
+        self.path = path  # tree verification: the accepted nodes
 
 
 def _verify_buffers(B, k):
@@ -230,3 +236,42 @@ def spec_verify(p, q, draft_tokens, seed: int, flag_window: float = FLAG_WINDOW)
                                 float(flag_window), _ptr(acc), _ptr(out), _ptr(mg), _ptr(fp),
                                 _ptr(fb))
     return VerifyResult(acc, out, mg, fp, fb, rc)
+
+
+def _tree_args(p, q, draft_tokens, parents):
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    B, n1, V = p.shape
+    n = n1 - 1
+    q = np.ascontiguousarray(q, dtype=np.float32).reshape(B, n, V)
+    x = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, n)
+    par = np.ascontiguousarray(parents, dtype=np.int32).reshape(B, n)
+    acc, out, mg, fp, fb = _verify_buffers(B, n)
+    path = np.zeros((B, n), dtype=np.int32)
+    return p, q, x, par, B, n, V, acc, out, mg, fp, fb, path
+
+
+def spec_verify_tree_given_uniforms(p, q, draft_tokens, parents, r, s,
+                                    flag_window: float = FLAG_WINDOW):
+    """Verification of a draft tree with explicit uniforms
+    (oracle.c: oracle_spec_verify_tree_given_uniforms).  p [B, n+1, V], q [B, n, V],
+    draft_tokens and parents [B, n] (parents[b, i]: the parent node of node i + 1, 0 for
+    the root); r [B, n], s [B, n+1]."""
+    lib = _load()
+    p, q, x, par, B, n, V, acc, out, mg, fp, fb, path = _tree_args(p, q, draft_tokens, parents)
+    r = np.ascontiguousarray(r, dtype=np.float64).reshape(B, n)
+    s = np.ascontiguousarray(s, dtype=np.float64).reshape(B, n + 1)
+    rc = lib.oracle_spec_verify_tree_given_uniforms(
+        _ptr(p), _ptr(q), _ptr(x), _ptr(par), _ptr(r), _ptr(s), B, n, V, float(flag_window),
+        _ptr(acc), _ptr(out), _ptr(path), _ptr(mg), _ptr(fp), _ptr(fb))
+    return VerifyResult(acc, out, mg, fp, fb, rc, path)
+
+
+def spec_verify_tree(p, q, draft_tokens, parents, seed: int, flag_window: float = FLAG_WINDOW):
+    """Philox uniforms + the tree walk (oracle.c: oracle_spec_verify_tree)."""
+    lib = _load()
+    p, q, x, par, B, n, V, acc, out, mg, fp, fb, path = _tree_args(p, q, draft_tokens, parents)
+    rc = lib.oracle_spec_verify_tree(_ptr(p), _ptr(q), _ptr(x), _ptr(par),
+                                     ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF), B, n, V,
+                                     float(flag_window), _ptr(acc), _ptr(out), _ptr(path),
+                                     _ptr(mg), _ptr(fp), _ptr(fb))
+    return VerifyResult(acc, out, mg, fp, fb, rc, path)

@@ -488,6 +488,179 @@ int oracle_spec_verify_given_uniforms(const float* p, const float* q, const int3
   return worst;
 }
 
+/* ------------------------------------------------------------------------------
+ * Verification of a draft tree (neuralmasteryai.com, "4. Tree Attention & Medusa
+ * Heads": several candidate paths verified in one pass; tempatgunting.com, "Draft
+ * Model Selection and Tree-Style Variants").  The pages stop at the mask; the walk is
+ * this reading of the modified rejection rule ("The Modified Rejection Sampling
+ * Algorithm"), applied to one candidate after another:
+ *  - nodes 1..n are the draft tokens, node 0 the root (the last context token);
+ *    parents[i] is the parent of node i + 1, in 0..i; draft[i] its token;
+ *  - p row u (of n + 1) is the target's distribution after node u; q row u (of n) the
+ *    distribution node u's children were drawn from, each independently;
+ *  - at node u the children are tried in increasing node order against a residual
+ *    that starts as p_u: child c (token x) is accepted iff r_c * S * q_u(x) <= R(x),
+ *    where R is the residual and S its total (taken as 1 for p_u itself); on a
+ *    rejection R becomes max(0, R - S * q_u) (the residual of the normalised R / S
+ *    against q_u, scaled back by S) and S its sum;
+ *  - an accepted child becomes u; when a node's children are all rejected, or it has
+ *    none, one token is drawn from R by inverse CDF (R = p_u when nothing was
+ *    rejected), and the walk ends.
+ * For a chain (parents[i] = i) this is exactly the rule of verify_one above, with the
+ * same uniforms: r_c = r[c - 1] (word 0 of counter (c - 1, b)), the draw at node u
+ * uses s[u] (word 1 of counter (u, b)).  A rejection that leaves a zero residual
+ * (impossible in exact arithmetic) falls back to drawing from p_u.
+ * Outputs per sequence: accepted_len (accepted draft tokens), out_tokens [n + 1] (the
+ * accepted path's tokens, the drawn token, then -1), path [n] (the accepted nodes,
+ * then -1), and the margin / flag of verify_one, the flag at the output position of
+ * the first decision whose uniform lies within flag_window of its threshold.
+ * ---------------------------------------------------------------------------- */
+static double residual_at(double p, double q, const double* S, int k) {
+  double r = p; /* R_0 = p, R_{i+1} = max(0, R_i - S_i q), S_0 = 1 */
+  for (int i = 0; i < k; ++i) {
+    const double d = r - S[i] * q;
+    r = d > 0.0 ? d : 0.0;
+  }
+  return r;
+}
+
+static int verify_tree_one(const float* pb, const float* qb, const int32_t* xb,
+                           const int32_t* par, const double* rb, const double* sb, int n, int V,
+                           double flag_window, double* w, double* S, int32_t* acc_out,
+                           int32_t* ob, int32_t* path, double* margin_out, int32_t* flag_out,
+                           int32_t* fallback_out) {
+  for (int t = 0; t <= n; ++t) ob[t] = -1;
+  for (int t = 0; t < n; ++t) path[t] = -1;
+  *acc_out = -1;
+  *margin_out = 0.0;
+  *flag_out = -1;
+  *fallback_out = 0;
+  for (int i = 0; i < n; ++i) {
+    if (par[i] < 0 || par[i] > i) return ORC_E_ARG;
+    if (xb[i] < 0 || xb[i] >= V) return ORC_E_TOKEN;
+  }
+  double mg = INFINITY;
+  int first_flag = -1, depth = 0, u = 0, fb = 0;
+  for (;;) {
+    const float* pu = pb + (size_t)u * V;
+    const float* qu = qb + (size_t)(u < n ? u : 0) * V;
+    int k = 0, next = -1;
+    S[0] = 1.0;
+    for (int c = u + 1; c <= n; ++c) {
+      if (par[c - 1] != u) continue;
+      const int x = xb[c - 1];
+      const double qx = (double)qu[x];
+      const double Rx = residual_at((double)pu[x], qx, S, k);
+      const double rc = rb[c - 1];
+      if (qx > 0.0) {
+        const double d = fabs(rc - Rx / (S[k] * qx));
+        if (d < mg) mg = d;
+        if (d < flag_window && first_flag < 0) first_flag = depth;
+      }
+      if (rc * S[k] * qx <= Rx) {
+        next = c;
+        break;
+      }
+      double sum = 0.0; /* the rejection's new residual and its total */
+      for (int y = 0; y < V; ++y) {
+        const double d = residual_at((double)pu[y], (double)qu[y], S, k) - S[k] * (double)qu[y];
+        sum += d > 0.0 ? d : 0.0;
+      }
+      S[++k] = sum;
+      if (sum == 0.0) {
+        fb = 1;
+        break;
+      }
+    }
+    if (next >= 0) {
+      ob[depth] = xb[next - 1];
+      path[depth] = next;
+      ++depth;
+      u = next;
+      continue;
+    }
+    /* Draw at node u from the residual (p_u after no rejection, or on the fallback). */
+    double tot = 0.0;
+    for (int y = 0; y < V; ++y) {
+      w[y] = (k == 0 || fb) ? (double)pu[y]
+                            : residual_at((double)pu[y], (double)qu[y], S, k);
+      tot += w[y];
+    }
+    if (!(tot > 0.0)) {
+      *acc_out = depth;
+      return ORC_E_DIST;
+    }
+    const double su = sb[u];
+    const double target = su * tot;
+    int drawn = -1;
+    double c = 0.0;
+    for (int y = 0; y < V; ++y) {
+      const double before = c;
+      c += w[y];
+      if (w[y] > 0.0 && c > target) {
+        drawn = y;
+        const double d = fmin(su - before / tot, c / tot - su);
+        if (d < mg) mg = d;
+        if (d < flag_window && first_flag < 0) first_flag = depth;
+        break;
+      }
+    }
+    if (drawn < 0) {
+      for (int y = V - 1; y >= 0; --y)
+        if (w[y] > 0.0) {
+          drawn = y;
+          break;
+        }
+      mg = 0.0;
+      if (first_flag < 0) first_flag = depth;
+    }
+    ob[depth] = drawn;
+    *acc_out = depth;
+    *margin_out = mg;
+    *flag_out = first_flag;
+    *fallback_out = fb;
+    return ORC_OK;
+  }
+}
+
+int oracle_spec_verify_tree_given_uniforms(const float* p, const float* q, const int32_t* draft,
+                                           const int32_t* parents, const double* r,
+                                           const double* s, int B, int n, int V,
+                                           double flag_window, int32_t* accepted_len,
+                                           int32_t* out_tokens, int32_t* path, double* margin,
+                                           int32_t* flag_pos, int32_t* fallback) {
+  if (B < 0 || n < 1 || V <= 0) return ORC_E_ARG;
+  int worst = ORC_OK;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    double* S = (double*)malloc(sizeof(double) * (size_t)(n + 2));
+    int local = (w && S) ? ORC_OK : ORC_E_ARG;
+#pragma omp for schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+      if (!w || !S) continue;
+      double mg;
+      int32_t fp, fbk;
+      const int rc = verify_tree_one(
+          p + (size_t)b * (n + 1) * V, q + (size_t)b * n * V, draft + (size_t)b * n,
+          parents + (size_t)b * n, r + (size_t)b * n, s + (size_t)b * (n + 1), n, V,
+          flag_window, w, S, accepted_len + b, out_tokens + (size_t)b * (n + 1),
+          path + (size_t)b * n, &mg, &fp, &fbk);
+      if (margin) margin[b] = mg;
+      if (flag_pos) flag_pos[b] = fp;
+      if (fallback) fallback[b] = fbk;
+      if (rc != ORC_OK && local == ORC_OK) local = rc;
+    }
+    free(w);
+    free(S);
+#pragma omp critical
+    {
+      if (local != ORC_OK && (worst == ORC_OK || local < worst)) worst = local;
+    }
+  }
+  return worst;
+}
+
 /* Full oracle: Philox uniforms followed by the rejection rule above. */
 int oracle_spec_verify(const float* p, const float* q, const int32_t* draft, uint64_t seed,
                        int B, int k, int V, double flag_window, int32_t* accepted_len,
@@ -505,6 +678,30 @@ int oracle_spec_verify(const float* p, const float* q, const int32_t* draft, uin
   const int rc = oracle_spec_verify_given_uniforms(p, q, draft, r, s, B, k, V, flag_window,
                                                    accepted_len, out_tokens, margin, flag_pos,
                                                    fallback);
+  free(r);
+  free(s);
+  return rc;
+}
+
+/* Full tree oracle: Philox uniforms (r[b][i] for node i + 1, s[b][u] for the draw at
+ * node u, as oracle_uniforms with k = n) followed by the walk above. */
+int oracle_spec_verify_tree(const float* p, const float* q, const int32_t* draft,
+                            const int32_t* parents, uint64_t seed, int B, int n, int V,
+                            double flag_window, int32_t* accepted_len, int32_t* out_tokens,
+                            int32_t* path, double* margin, int32_t* flag_pos,
+                            int32_t* fallback) {
+  if (B < 0 || n < 1 || V <= 0) return ORC_E_ARG;
+  double* r = (double*)malloc(sizeof(double) * ((size_t)B * n + 1));
+  double* s = (double*)malloc(sizeof(double) * ((size_t)B * (n + 1) + 1));
+  if (!r || !s) {
+    free(r);
+    free(s);
+    return ORC_E_ARG;
+  }
+  oracle_uniforms(seed, B, n, r, s);
+  const int rc = oracle_spec_verify_tree_given_uniforms(p, q, draft, parents, r, s, B, n, V,
+                                                        flag_window, accepted_len, out_tokens,
+                                                        path, margin, flag_pos, fallback);
   free(r);
   free(s);
   return rc;
