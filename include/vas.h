@@ -55,6 +55,7 @@ typedef struct CUstream_st* vas_stream_t; /* identical to cudaStream_t */
 #define VAS_DEV_BAD_TOKEN 0x4      /* draft token outside [0, V)                       */
 #define VAS_DEV_EMPTY_ROW 0x8      /* the row to draw from has no positive mass        */
 #define VAS_DEV_TIMEOUT 0x10       /* a bounded in-kernel wait gave up                 */
+#define VAS_DEV_BAD_TREE 0x20      /* spec_verify_tree: a parent outside 0..node - 1     */
 #define VAS_DEV_RESIDUAL_FALLBACK 0x100 /* informational: a zero residual after a       */
                                         /* rejection; the token was drawn from p_j      */
 
@@ -251,6 +252,37 @@ int spec_verify(const float* p, const float* q, const int32_t* draft_tokens, uin
 /* Synchronises `stream`, then returns (and clears) the device error word of the
  * current device in *bits.  Returns VAS_OK or VAS_E_CUDA. */
 int vas_last_device_error(int32_t* bits, vas_stream_t stream);
+
+/* Verification of a draft tree.
+ *
+ * Defined by: "Continuous Batching & Speculative Decoding" (neuralmasteryai.com),
+ * section "4. Tree Attention & Medusa Heads" -- candidate paths verified in one pass --
+ * and section "The Modified Rejection Sampling Algorithm", applied to a node's
+ * children in turn (the pages give no rule for several candidates; this reading keeps
+ * the output distribution equal to p when each child of a node was drawn
+ * independently from that node's q row).
+ *
+ * Per sequence b: nodes 1..n are draft tokens, node 0 is the root (the last context
+ * token).  parents[b][i] is the parent of node i + 1, in 0..i; draft_tokens[b][i] its
+ * token.  p[b][u] ([B, n+1, V] fp32) is the target's distribution after node u;
+ * q[b][u] ([B, n, V] fp32) the distribution node u's children were drawn from.
+ * Walk: at node u the children are tried in node order against a residual R (first
+ * p_u) with total S (first 1): child c with token x is accepted iff
+ * r_c * S * q_u(x) <= R(x), r_c = (word 0 of Philox(c - 1, b)) per spec_verify; a
+ * rejection makes R = max(0, R - S * q_u) and S its sum.  An accepted child becomes u.
+ * When a node's children are all rejected, or it has none, one token is drawn from R
+ * by inverse CDF with word 1 of Philox(u, b) (from p_u when a rejection leaves a zero
+ * residual: VAS_DEV_RESIDUAL_FALLBACK) and the walk ends.  For a chain (parents[b][i]
+ * = i) this is exactly spec_verify.
+ * Outputs: accepted_len[b] (accepted draft tokens), out_tokens[b] ([n+1]: the accepted
+ * tokens, the drawn token, then -1), path[b] ([n]: the accepted nodes, then -1).
+ * n in 1..255.  Errors: VAS_E_INVALID_ARG on the host; device: VAS_DEV_BAD_TOKEN or
+ * VAS_DEV_BAD_TREE (the sequence emits accepted_len = -1 and all -1), VAS_DEV_EMPTY_ROW.
+ */
+int spec_verify_tree(const float* p, const float* q, const int32_t* draft_tokens,
+                     const int32_t* parents, uint64_t seed, int32_t* accepted_len,
+                     int32_t* out_tokens, int32_t* path, int32_t B, int32_t n, int32_t V,
+                     vas_stream_t stream);
 
 /* Diagnostic: the device Philox4x32-10 used by spec_verify, exposed for testing.
  * counters [n, 4] and out [n, 4] are device uint32 arrays; key = (key0, key1). */

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libvas.so")
-SOURCES = ["abi.cu", "paged_attn.cu", "spec_verify.cu", "static_ws.cu", "pool.cpp"]
+SOURCES = ["abi.cu", "paged_attn.cu", "spec_verify.cu", "spec_verify_tree.cu", "static_ws.cu",
+           "pool.cpp"]
 HEADERS = ["device_util.cuh", "philox.cuh", "vas_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -38,6 +38,7 @@ VAS_DEV_BAD_LENGTHS = 0x2
 VAS_DEV_BAD_TOKEN = 0x4
 VAS_DEV_EMPTY_ROW = 0x8
 VAS_DEV_TIMEOUT = 0x10
+VAS_DEV_BAD_TREE = 0x20
 VAS_DEV_RESIDUAL_FALLBACK = 0x100
 VAS_F32 = 0
 VAS_BF16 = 1
@@ -65,6 +66,8 @@ _sig = {
     "paged_attn_fwd_quant": ([_c_void_p] * 11 + [_P_dims, _c_void_p, _sz, _c_void_p], ctypes.c_int),
     "spec_verify": ([_c_void_p, _c_void_p, _c_void_p, _u64, _c_void_p, _c_void_p, _i32, _i32, _i32,
                      _c_void_p], ctypes.c_int),
+    "spec_verify_tree": ([_c_void_p] * 4 + [_u64] + [_c_void_p] * 3 + [_i32, _i32, _i32, _c_void_p],
+                         ctypes.c_int),
     "vas_last_device_error": ([ctypes.POINTER(_i32), _c_void_p], ctypes.c_int),
     "vas_philox4x32_10": ([_c_void_p, _u32, _u32, _c_void_p, _i64, _c_void_p], ctypes.c_int),
     "vas_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -218,6 +221,22 @@ def paged_attn_fwd_quant(q, k_pages, v_pages, k_scale, v_scale, block_table, seq
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream))
     _check("paged_attn_fwd_quant", st)
+
+
+def spec_verify_tree(p, q, draft_tokens, parents, seed: int, accepted_len, out_tokens, path, *,
+                     stream=None) -> None:
+    """Verification of a draft tree (include/vas.h: spec_verify_tree).  p [B, n+1, V] fp32,
+    q [B, n, V] fp32, draft_tokens and parents [B, n] int32 -> accepted_len [B],
+    out_tokens [B, n+1], path [B, n]."""
+    B, n1, V = p.shape
+    st = _lib.spec_verify_tree(_dev(p, "p", torch.float32), _dev(q, "q", torch.float32),
+                               _dev(draft_tokens, "draft_tokens", torch.int32),
+                               _dev(parents, "parents", torch.int32),
+                               ctypes.c_uint64(seed & (2**64 - 1)),
+                               _dev(accepted_len, "accepted_len", torch.int32),
+                               _dev(out_tokens, "out_tokens", torch.int32),
+                               _dev(path, "path", torch.int32), B, n1 - 1, V, _stream_ptr(stream))
+    _check("spec_verify_tree", st)
 
 
 def spec_verify(p, q, draft_tokens, seed: int, accepted_len, out_tokens, *, stream=None) -> None:
