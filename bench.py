@@ -118,11 +118,22 @@ def elem_sizes(kv_dtype):
     return (2, 2) if kv_dtype == wl.BF16 else (4, 4)
 
 
+def tree_verify_bytes(accepted_len, path, parents, V):
+    """As verify_bytes for draft trees: the walk ends at node u (the last accepted node,
+    or the root); with children, its p and q rows (the residual), else its p row."""
+    rows = 0
+    n = parents.shape[1]
+    for b, acc in enumerate(np.asarray(accepted_len)):
+        u = int(path[b, acc - 1]) if acc > 0 else 0
+        rows += 2 if np.any(parents[b] == u) else 1
+    return int(rows * V * 4 + len(accepted_len) * (n * 4 * 3 + n * 8 + (n + 1) * 4 + 4))
+
+
 def workload_desc(name):
     from verify_attention_spec_gb300 import workloads as wl
     w = wl.WORKLOADS[name]
     return (f"{name}: {w.num_seqs} seqs ({w.num_seqs - w.num_verify} decode + {w.num_verify} "
-            f"verify k={w.k}), Hq/Hkv {w.num_q_heads}/{w.num_kv_heads}, d {w.head_dim}, "
+            f"verify {'trees of ' if w.tree else ''}k={w.k}), Hq/Hkv {w.num_q_heads}/{w.num_kv_heads}, d {w.head_dim}, "
             f"{w.kv_dtype}, page {w.page_size}, lengths {w.length_law}{w.length_args or w.fixed_lens}; "
             f"spec_verify vocab {w.vocab}")
 
@@ -211,8 +222,9 @@ def ncu_traffic(workload):
 # ---------------------------------------------------------------------------------
 # The oracle on the host cores (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------------
-def oracle_sample(a, seqs):
-    """Host copy of the chosen sequences with a compact pool (oracle input)."""
+def oracle_sample(a, seqs, parents=None):
+    """Host copy of the chosen sequences with a compact pool (oracle input); parents:
+    the batch's draft trees (per query row), sliced to the chosen rows."""
     import torch
     from verify_attention_spec_gb300 import workloads as wl
     bt = a.block_table.cpu().numpy()
@@ -233,14 +245,15 @@ def oracle_sample(a, seqs):
     for r, x in enumerate(nbt):
         btn[r, :len(x)] = x
     r = torch.from_numpy(np.concatenate(rows)).to(a.q.device)
+    par = None if parents is None else np.asarray(parents)[np.concatenate(rows)]
     if a.kv_dtype in wl.QUANTIZED:
         np_ = lambda t: t.detach().cpu().contiguous().numpy()
         return dict(q=wl.bf16_bits(a.q[r].cpu()), k=np_(a.k_pages[idx]), v=np_(a.v_pages[idx]),
                     ks=np_(a.k_scale[idx]), vs=np_(a.v_scale[idx]), bt=btn, lens=lens[seqs],
-                    qlens=qlens[seqs])
+                    qlens=qlens[seqs], parents=par)
     st = lambda t: wl.storage_for_oracle(t, a.kv_dtype)
     return dict(q=st(a.q[r]), k=st(a.k_pages[idx]), v=st(a.v_pages[idx]), bt=btn,
-                lens=lens[seqs], qlens=qlens[seqs])
+                lens=lens[seqs], qlens=qlens[seqs], parents=par)
 
 
 def run_oracle_attention(sample, kv_dtype):
@@ -250,10 +263,20 @@ def run_oracle_attention(sample, kv_dtype):
         fmt = oracle.Q_E4M3 if kv_dtype == wl.FP8 else oracle.Q_INT8
         return oracle.paged_attn_quant(sample["q"], sample["k"], sample["v"], sample["ks"],
                                        sample["vs"], sample["bt"], sample["lens"], sample["qlens"],
-                                       fmt=fmt)
+                                       fmt=fmt, parents=sample["parents"])
     code = oracle.BF16 if kv_dtype == wl.BF16 else oracle.F32
     return oracle.paged_attn(sample["q"], sample["k"], sample["v"], sample["bt"], sample["lens"],
-                             sample["qlens"], dtype_code=code)
+                             sample["qlens"], dtype_code=code, parents=sample["parents"])
+
+
+def run_oracle_verify(v, rows=None):
+    """The oracle's verification of v (its first `rows` sequences): the tree walk when v
+    holds trees, else the plain rule."""
+    import oracle
+    sl = slice(None) if rows is None else slice(0, rows)
+    if v.parents is not None:
+        return oracle.spec_verify_tree(v.p[sl], v.q[sl], v.draft[sl], v.parents[sl], v.seed)
+    return oracle.spec_verify(v.p[sl], v.q[sl], v.draft[sl], v.seed)
 
 
 def time_oracle_attention(sample, kv_dtype):
@@ -262,24 +285,24 @@ def time_oracle_attention(sample, kv_dtype):
     return time.perf_counter() - t0
 
 
-def choose_oracle_sample(a, target_s, rng_seed=0):
+def choose_oracle_sample(a, target_s, rng_seed=0, parents=None):
     """Grow a seeded random sample of sequences (doubling) until the oracle takes at
     least target_s seconds on it, or the batch is exhausted."""
     order = np.random.default_rng(rng_seed).permutation(a.num_seqs)
     n = 4
     while True:
         seqs = sorted(order[:n].tolist())
-        smp = oracle_sample(a, seqs)
+        smp = oracle_sample(a, seqs, parents)
         dt = time_oracle_attention(smp, a.kv_dtype)
         if dt >= target_s or n >= a.num_seqs:
             return seqs, smp, dt
         n = min(a.num_seqs, max(n * 2, int(n * target_s / max(dt, 1e-3) * 1.1)))
 
 
-def cpu_baseline(a, v, name):
+def cpu_baseline(a, v, name, parents=None):
     import oracle
     w = a
-    seqs, smp, dt = choose_oracle_sample(a, 10.0)
+    seqs, smp, dt = choose_oracle_sample(a, 10.0, parents=parents)
     runs = 1
     if dt < 10.0:  # the whole batch takes less than the target: run it again
         extra = int(np.ceil(10.0 / max(dt, 1e-3))) - 1
@@ -293,7 +316,7 @@ def cpu_baseline(a, v, name):
                      f"{runs} run(s) ({by / 1e9:.3f} GB algorithmic, {dt:.1f} s)"}
     if v is not None:
         t0 = time.perf_counter()
-        oracle.spec_verify(v.p, v.q, v.draft, v.seed)
+        run_oracle_verify(v)
         tv = time.perf_counter() - t0
         out["spec_verify_seqs_per_s"] = v.B / tv
         out["sample"] += f"; spec_verify on all {v.B} verify sequences ({tv:.2f} s)"
@@ -368,18 +391,31 @@ def run_ours(args):
                            a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype,
                            mv(a.k_scale), mv(a.v_scale))
     quant = a.kv_dtype if a.kv_dtype in wl.QUANTIZED else None
-    v = wl.workload_verify(name)
+    # Draft trees (tree workloads): one random tree per verify window, its ancestor
+    # masks for the attention and its nodes for the verification.
+    tree_masks = None
+    attn_parents = None
+    if w.tree:
+        qlens_all = a.query_lens.cpu().numpy()
+        attn_parents = wl.draft_tree_parents(qlens_all, seed=w.seed)
+        tree_masks = torch.from_numpy(wl.ancestor_bits(attn_parents, qlens_all).view(np.int64)).to(dev)
+    v = wl.workload_verify(name, attn_parents=attn_parents) if not args.max_seqs or not w.tree else None
     if args.max_seqs and v is not None:
         nv = max(1, int((qlens > 1).sum()))
-        v = wl.VerifyInputs(v.p[:nv], v.q[:nv], v.draft[:nv], v.seed)
+        v = wl.VerifyInputs(v.p[:nv], v.q[:nv], v.draft[:nv], v.seed,
+                            None if v.parents is None else v.parents[:nv])
     dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens, quant=quant)
     ws = vas.alloc_workspace(dims, device=dev)
 
     def attn(q_, bt_, sl_, ql_, out_, lse_):
-        """One attention call through the C ABI (quantised pools: paged_attn_fwd_quant)."""
+        """One attention call through the C ABI (quantised pools: paged_attn_fwd_quant;
+        draft trees: paged_attn_fwd_tree)."""
         if quant:
             vas.paged_attn_fwd_quant(q_, a.k_pages, a.v_pages, a.k_scale, a.v_scale, bt_, sl_, ql_,
-                                     out_, lse_, ws, quant=quant, dims=dims)
+                                     out_, lse_, ws, quant=quant, tree_mask=tree_masks, dims=dims)
+        elif tree_masks is not None:
+            vas.paged_attn_fwd_tree(q_, a.k_pages, a.v_pages, bt_, sl_, ql_, tree_masks, out_,
+                                    lse_, ws, dims=dims)
         else:
             vas.paged_attn_fwd(q_, a.k_pages, a.v_pages, bt_, sl_, ql_, out_, lse_, ws, dims=dims)
 
@@ -391,11 +427,20 @@ def run_ours(args):
         x_d = torch.from_numpy(v.draft).to(dev)
         acc_d = torch.empty(v.B, dtype=torch.int32, device=dev)
         tok_d = torch.empty(v.B, v.k + 1, dtype=torch.int32, device=dev)
+        par_d = torch.from_numpy(v.parents).to(dev) if v.parents is not None else None
+        path_d = torch.empty(v.B, v.k, dtype=torch.int32, device=dev)
+
+    def verify(p_, q_, x_, acc_, tok_):
+        """One verification call through the C ABI (draft trees: spec_verify_tree)."""
+        if par_d is not None:
+            vas.spec_verify_tree(p_, q_, x_, par_d, v.seed, acc_, tok_, path_d)
+        else:
+            vas.spec_verify(p_, q_, x_, v.seed, acc_, tok_)
 
     def step():
         attn(a.q, a.block_table, a.seq_lens, a.query_lens, out, lse)
         if v is not None:
-            vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
+            verify(p_d, q_d, x_d, acc_d, tok_d)
 
     elem, kv_elem = elem_sizes(a.kv_dtype)
     a_bytes = attn_bytes(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
@@ -410,7 +455,12 @@ def run_ours(args):
     a_bytes_unique = a_bytes - kv_logical + kv_unique
     step()
     torch.cuda.synchronize()
-    v_bytes = verify_bytes(acc_d.cpu().numpy(), v.k, v.V) if v is not None else 0
+    if v is None:
+        v_bytes = 0
+    elif v.parents is not None:
+        v_bytes = tree_verify_bytes(acc_d.cpu().numpy(), path_d.cpu().numpy(), v.parents, v.V)
+    else:
+        v_bytes = verify_bytes(acc_d.cpu().numpy(), v.k, v.V)
     step_bytes = a_bytes + v_bytes
 
     for _ in range(args.warmup):
@@ -431,7 +481,7 @@ def run_ours(args):
         attn(a.q, a.block_table, a.seq_lens, a.query_lens, out, lse)
         ev[i][1].record()
         if v is not None:
-            vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
+            verify(p_d, q_d, x_d, acc_d, tok_d)
         ev[i][2].record()
     t_end.record()
     torch.cuda.synchronize()
@@ -479,8 +529,7 @@ def run_ours(args):
             q_, bt_, sl_, ql_ = sl["din"]
             attn(q_, bt_, sl_, ql_, sl["dout"][0], sl["dout"][1])
             if v is not None:
-                vas.spec_verify(sl["dv"][0], sl["dv"][1], sl["dv"][2], v.seed, sl["dout"][2],
-                                sl["dout"][3])
+                verify(sl["dv"][0], sl["dv"][1], sl["dv"][2], sl["dout"][2], sl["dout"][3])
             sl["comp"].record(cs)
 
         def download(sl):
@@ -575,7 +624,7 @@ def run_ours(args):
     if e2e is not None:
         res["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(a, v, name)
+        res["cpu_baseline"] = cpu_baseline(a, v, name, attn_parents)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -595,7 +644,8 @@ def run_reference(args):
     name = args.workload
     w = wl.WORKLOADS[name]
     # the inputs: the same workload, its pool drawn on the host (no GPU on this leg)
-    lens, qlens = wl.sample_lengths(w), wl.query_lengths(w)
+    lens, qlens = wl.sample_lengths(w) + w.prefix_tokens, wl.query_lengths(w)
+    parents_all = wl.draft_tree_parents(qlens, seed=w.seed) if w.tree else None
     order = np.random.default_rng(0).permutation(len(lens))
     # a bounded sample: sequences in seeded order up to ~64 MB of KV
     elem, kv_elem = elem_sizes(w.kv_dtype)
@@ -610,15 +660,19 @@ def run_reference(args):
     a = wl.attention_inputs(lens[seqs], qlens[seqs], num_q_heads=w.num_q_heads,
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, kv_dtype=w.kv_dtype, seed=w.seed)
-    v = wl.workload_verify(name)
-    smp = oracle_sample(a, list(range(len(seqs))))
+    v = wl.workload_verify(name, attn_parents=parents_all)
+    par = None
+    if parents_all is not None:
+        row0 = np.concatenate([[0], np.cumsum(qlens)])
+        par = np.concatenate([parents_all[row0[i]:row0[i + 1]] for i in seqs])
+    smp = oracle_sample(a, list(range(len(seqs))), par)
     by = attn_bytes(smp["lens"], smp["qlens"], w.num_q_heads, w.num_kv_heads, w.head_dim,
                     w.page_size, elem, kv_elem)
 
     def step():
         run_oracle_attention(smp, w.kv_dtype)
         if v is not None:
-            oracle.spec_verify(v.p[:8], v.q[:8], v.draft[:8], v.seed)
+            run_oracle_verify(v, rows=8)
 
     for _ in range(args.warmup):
         step()

@@ -85,6 +85,7 @@ class Workload:
     fixed_qlens: Optional[tuple] = None
     prefix_tokens: int = 0     # a shared prefix (whole pages) added to every sequence ...
     prefix_group: int = 0      # ... shared by consecutive groups of this many sequences
+    tree: bool = False         # the verify windows are draft trees (k nodes under the root)
 
 
 WORKLOADS = {
@@ -107,6 +108,11 @@ WORKLOADS = {
 # the same 64 prompt pages).
 WORKLOADS["shared70b"] = dataclasses.replace(WORKLOADS["stress70b"], name="shared70b",
                                              prefix_tokens=2048, prefix_group=8)
+# Draft trees: the 70B batch whose 64 verify sequences each bring a random 16-node draft
+# tree under the last context token (17 query tokens), attention with tree masks and
+# tree verification over vocab 128256.
+WORKLOADS["tree70b"] = dataclasses.replace(WORKLOADS["stress70b"], name="tree70b", k=16,
+                                           tree=True)
 for _base in ("stress70b", "decode64"):
     for _q in QUANTIZED:
         WORKLOADS[f"{_base}_{_q}"] = dataclasses.replace(WORKLOADS[_base], name=f"{_base}_{_q}",
@@ -324,6 +330,7 @@ class VerifyInputs:
     q: np.ndarray          # float32 [B, k, V] draft probabilities
     draft: np.ndarray      # int32 [B, k] draft tokens, x_i ~ q_i
     seed: int              # Philox seed of the call
+    parents: Optional[np.ndarray] = None  # int32 [B, k]: draft trees (node i + 1's parent)
 
     @property
     def B(self):
@@ -364,10 +371,60 @@ def verify_inputs(B: int, k: int, V: int, *, seed: int, p_logit_std: float = 3.0
     return VerifyInputs(p, q, draft, seed)
 
 
-def workload_verify(name: str) -> Optional[VerifyInputs]:
+def tree_verify_inputs(parents: np.ndarray, V: int, *, seed: int, p_logit_std: float = 3.0,
+                       q_noise_std: float = 1.5) -> VerifyInputs:
+    """Synthetic rows for verifying draft trees: parents [B, n] (node i + 1 hangs under
+    node parents[b, i], 0 the root); p [B, n+1, V] and q [B, n, V] as in verify_inputs,
+    node i + 1's token drawn from q row parents[b, i] (its parent's draft distribution)."""
+    B, n = parents.shape
+    rng = _rng(seed, 6)
+    p = np.empty((B, n + 1, V), dtype=np.float32)
+    q = np.empty((B, n, V), dtype=np.float32)
+    draft = np.empty((B, n), dtype=np.int32)
+    for b in range(B):
+        logits = rng.normal(0.0, p_logit_std, size=(n + 1, V))
+        p[b] = _softmax_rows(logits)
+        q64 = _softmax_rows(logits[:n] + rng.normal(0.0, q_noise_std, size=(n, V)))
+        q[b] = q64
+        for i in range(n):
+            row = q64[parents[b, i]]
+            draft[b, i] = rng.choice(V, p=row / row.sum())
+    return VerifyInputs(p, q, draft, seed)
+
+
+def ancestor_bits(parents: np.ndarray, qlens) -> np.ndarray:
+    """The attention kernel's tree encoding: per query token a uint64 with bit a set for
+    every proper ancestor a among its window's tokens (parents as in
+    draft_tree_parents)."""
+    masks = np.zeros(len(parents), dtype=np.uint64)
+    row0 = 0
+    for ql in np.asarray(qlens, dtype=np.int64):
+        for j in range(int(ql)):
+            m, a = 0, int(parents[row0 + j])
+            while a >= 0:
+                m |= 1 << a
+                a = int(parents[row0 + a])
+            masks[row0 + j] = m
+        row0 += int(ql)
+    return masks
+
+
+def workload_verify(name: str, attn_parents: Optional[np.ndarray] = None) -> Optional[VerifyInputs]:
+    """The workload's verification inputs.  For a tree workload, attn_parents are the
+    query windows' trees (draft_tree_parents of the query lengths): each verify window's
+    nodes 1..k hang where its query tokens 1..k do."""
     w = WORKLOADS[name]
     if not w.vocab:
         return None
+    if w.tree:
+        qlens = query_lengths(w)
+        row0 = np.concatenate([[0], np.cumsum(qlens)])
+        verify = [i for i in range(len(qlens)) if qlens[i] > 1]
+        par = np.stack([attn_parents[row0[i] + 1:row0[i + 1]] for i in verify]).astype(np.int32)
+        par = np.maximum(par, 0)
+        v = tree_verify_inputs(par, w.vocab, seed=w.seed, p_logit_std=w.p_logit_std,
+                               q_noise_std=w.q_noise_std)
+        return dataclasses.replace(v, parents=par)
     return verify_inputs(w.num_verify, w.k, w.vocab, seed=w.seed, p_logit_std=w.p_logit_std,
                          q_noise_std=w.q_noise_std)
 
