@@ -13,16 +13,19 @@
 // For a chain this is spec_verify's rule with its uniforms: r_c is word 0 of
 // Philox(c - 1, b), the draw at node u uses word 1 of Philox(u, b).
 //
-// Kernel: one CTA of 512 threads per sequence; thread 0 takes the decisions, the CTA
-// makes the passes over the vocabulary.  A pass covers the row in tiles of 256
-// consecutive elements, 8 contiguous per lane: each lane sums its 8 weights, the warp
-// scans the 32 lane sums (fp32, lane order) and the last lane's value is the tile's
-// total, kept in shared memory; tile totals add up in fp64.  The residual's new total
-// is the sum of the tile totals; a draw walks the tile totals to the tile where the
-// inverse CDF crosses its target, repeats that tile's scan and walks the crossing
-// lane's 8 elements.  Weights are fp32 (R_k recomputed per element from p, q and
-// S_0..S_{k-1}); totals and thresholds are fp64 (this part's fp64 rate is too low for
-// fp64 per element).
+// Kernel: one thread-block cluster of C CTAs per sequence (C <= 8, fewer for small
+// vocabularies); CTA r owns slice r of the vocabulary.  Every CTA takes the same
+// decisions (thread 0, from the same values), so the clusters' CTAs walk in step.  A
+// pass covers each slice in tiles of 256 consecutive elements, 8 contiguous per lane:
+// each lane sums its 8 weights, the warp scans the 32 lane sums (fp32, lane order) and
+// the last lane's value is the tile's total, kept in shared memory; tile totals add up
+// in fp64 to the slice total, published to the cluster, and every CTA adds the C slice
+// totals in rank order.  A draw finds the slice, then the tile where the inverse CDF
+// crosses its target; that CTA repeats the tile's scan and walks the crossing lane's 8
+// elements.  Weights are fp32 (R_k recomputed per element from p, q and S_0..S_{k-1});
+// totals and thresholds are fp64 (this part's fp64 rate is too low for fp64 per
+// element).
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,10 +35,12 @@
 #include "philox.cuh"
 #include "vas_internal.h"
 
+namespace cg = cooperative_groups;
+
 namespace vas {
 namespace verify_tree {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNodes = 255;  // draft nodes per sequence (node indices fit in a byte)
 
@@ -47,7 +52,7 @@ struct Args {
   int32_t* accepted_len;   // [B]
   int32_t* out_tokens;     // [B, n + 1]
   int32_t* path;           // [B, n]
-  int32_t B, n, V;
+  int32_t B, n, V, slice;  // slice: vocabulary elements per CTA (multiple of kTile)
   uint32_t key0, key1;
   int32_t* err;
 };
@@ -69,7 +74,10 @@ __device__ __forceinline__ float weight(float p, float q, const float* S, int k,
 
 constexpr int kLaneElems = 8;
 constexpr int kTile = 32 * kLaneElems;
-constexpr int kMaxTiles = (128256 * 2 + kTile - 1) / kTile;  // vocabularies up to 256512
+constexpr int kMaxCluster = 8;
+constexpr int kSliceMin = 4096;     // smallest vocabulary slice per CTA
+constexpr int kMaxTiles = 160;      // tiles per slice: vocabularies up to 8 x 160 x 256
+constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTiles * kTile;
 
 // One lane's 8 inputs from x0 (past V: zero), as two float4 loads per row when the
 // rows are 16-byte aligned and the 8 elements lie inside the row.
@@ -121,13 +129,14 @@ __device__ __forceinline__ float warp_inclusive_scan(float v) {
   return v;
 }
 
-// A pass: every tile's total into s_tile[]; returns the row total (every thread)
-// and the last element with positive weight (thread 0's *last).
-__device__ double pass_totals(const float* pu, const float* qu, int V, const float* S, int k,
-                              bool from_p, bool next, double* s_tile, int* s_last,
+// A pass over this CTA's slice [xb, V' = min(V, xb + slice)): every tile's total into
+// s_tile[]; returns the slice total (every thread) and leaves the slice's last element
+// with positive weight in *s_last.
+__device__ double pass_totals(const float* pu, const float* qu, int xb, int V, const float* S,
+                              int k, bool from_p, bool next, double* s_tile, int* s_last,
                               double* s_total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n_tiles = (V + kTile - 1) / kTile;
+  const int n_tiles = (V - xb + kTile - 1) / kTile;
   const bool vec = ((reinterpret_cast<uintptr_t>(pu) | reinterpret_cast<uintptr_t>(qu)) & 15) == 0;
   if (threadIdx.x == 0) *s_last = -1;
   __syncthreads();
@@ -138,13 +147,13 @@ __device__ double pass_totals(const float* pu, const float* qu, int V, const flo
     float p8[4][kLaneElems], q8[4][kLaneElems];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int x0 = (t0 + j) * kTile + lane * kLaneElems;
+      const int x0 = xb + (t0 + j) * kTile + lane * kLaneElems;
       if (t0 + j < n_tiles) lane_load(pu, qu, x0, V, vec, p8[j], q8[j]);
     }
     float v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int x0 = (t0 + j) * kTile + lane * kLaneElems;
+      const int x0 = xb + (t0 + j) * kTile + lane * kLaneElems;
       v[j] = 0.f;
       if (t0 + j < n_tiles)
 #pragma unroll
@@ -173,16 +182,22 @@ __device__ double pass_totals(const float* pu, const float* qu, int V, const flo
   return *s_total;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Args a) {
-  const int b = blockIdx.x;
+__global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Args a) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = a.n, V = a.V;
+  const int xb = min(V, rank * a.slice), xe = min(V, xb + a.slice);  // this CTA's slice
   __shared__ int32_t s_par[kMaxNodes], s_x[kMaxNodes];
   __shared__ double s_S[kMaxNodes + 1];
   __shared__ float s_Sf[kMaxNodes + 1];
   __shared__ double s_tile[kMaxTiles];
-  __shared__ double s_total;
-  __shared__ int32_t s_bad, s_accept, s_tile_hit, s_found, s_last;
+  __shared__ double s_total, s_pub[2];   // slice total; published, by pass parity
+  __shared__ int32_t s_last, s_pub_last[2];
+  __shared__ int32_t s_bad, s_accept, s_tile_hit, s_found;
+  __shared__ double s_target, s_before;
   pdl_wait_prior_grid();  // inputs written by the previous kernel in the stream are visible
 
   if (tid == 0) s_bad = 0;
@@ -198,21 +213,46 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
   __syncthreads();
   int32_t* out = a.out_tokens + (size_t)b * (n + 1);
   int32_t* path = a.path + (size_t)b * n;
-  for (int t = tid; t <= n; t += kThreads) out[t] = -1;
-  for (int t = tid; t < n; t += kThreads) path[t] = -1;
-  if (s_bad) {
-    if (tid == 0) {
+  if (rank == 0) {
+    for (int t = tid; t <= n; t += kThreads) out[t] = -1;
+    for (int t = tid; t < n; t += kThreads) path[t] = -1;
+  }
+  if (s_bad) {  // the same in every CTA of the cluster: all leave before any barrier
+    if (rank == 0 && tid == 0) {
       a.accepted_len[b] = -1;
       atomicOr(a.err, (s_bad & 1 ? VAS_DEV_BAD_TOKEN : 0) | (s_bad & 2 ? VAS_DEV_BAD_TREE : 0));
     }
     return;
   }
 
+  int pp = 0;  // publication slot: passes alternate, one cluster barrier each
+  // A pass over the slices; returns the row total, identical in every CTA (slice
+  // totals added in rank order), and the row's last element with weight in *last.
+  auto cluster_pass = [&](const float* pu, const float* qu, int k, bool from_p, bool next,
+                          int* last) -> double {
+    const double mine = pass_totals(pu, qu, xb, xe, s_Sf, k, from_p, next, s_tile, &s_last,
+                                    &s_total);
+    if (tid == 0) {
+      s_pub[pp] = mine;
+      s_pub_last[pp] = s_last;
+    }
+    cluster.sync();  // every slice total of this pass is published
+    double all = 0.0;
+    int lst = -1;
+    for (int r = 0; r < C; ++r) {
+      all += *cluster.map_shared_rank(&s_pub[pp], r);
+      lst = max(lst, *cluster.map_shared_rank(&s_pub_last[pp], r));
+    }
+    pp ^= 1;
+    *last = lst;
+    return all;
+  };
+
   int u = 0, depth = 0;
   for (;;) {
     const float* pu = a.p + ((size_t)b * (n + 1) + u) * V;
     const float* qu = a.q + ((size_t)b * n + (u < n ? u : 0)) * V;
-    int k = 0, next = -1;
+    int k = 0, next = -1, last = -1;
     bool fallback = false;
     if (tid == 0) {
       s_S[0] = 1.0;
@@ -236,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
         break;
       }
       // Rejected: the new residual's total.
-      const double total = pass_totals(pu, qu, V, s_Sf, k, false, true, s_tile, &s_last, &s_total);
+      const double total = cluster_pass(pu, qu, k, false, true, &last);
       ++k;
       if (tid == 0) {
         s_S[k] = total;
@@ -249,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
       }
     }
     if (next >= 0) {
-      if (tid == 0) {
+      if (rank == 0 && tid == 0) {
         out[depth] = s_x[next - 1];
         path[depth] = next;
       }
@@ -259,25 +299,35 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
     }
     // Draw at node u: from R_k, or from p_u (nothing rejected, or the fallback).
     const bool from_p = k == 0 || fallback;
-    const double total = pass_totals(pu, qu, V, s_Sf, k, from_p, false, s_tile, &s_last, &s_total);
-    const int n_tiles = (V + kTile - 1) / kTile;
-    double target = 0.0;
-    if (total > 0.0) {
-      const uint4 w4 = philox4x32_10(make_uint4((uint32_t)u, (uint32_t)b, 0u, 0u), a.key0, a.key1);
-      target = philox_uniform(w4.y) * total;
-    }
+    const double total = cluster_pass(pu, qu, k, from_p, false, &last);
     if (tid == 0) {
-      // The tile where the running total passes the target (tiles in order).
       s_tile_hit = -1;
       s_found = -1;
-      double c = 0.0;
-      for (int t = 0; t < n_tiles && total > 0.0; ++t) {
-        if (c + s_tile[t] > target) {
-          s_tile_hit = t;
-          s_total = c;  // the total before the tile
-          break;
+      if (total > 0.0) {
+        const uint4 w4 = philox4x32_10(make_uint4((uint32_t)u, (uint32_t)b, 0u, 0u), a.key0,
+                                       a.key1);
+        const double target = philox_uniform(w4.y) * total;
+        // The slice (rank order, as the total was formed), then the tile, where the
+        // running total passes the target.
+        double c = 0.0;
+        int owner = -1;
+        for (int r = 0; r < C; ++r) {
+          const double t = *cluster.map_shared_rank(&s_pub[pp ^ 1], r);
+          if (owner < 0 && c + t > target) owner = r;
+          if (owner < 0) c += t;
         }
-        c += s_tile[t];
+        if (owner == rank) {
+          const int n_tiles = (xe - xb + kTile - 1) / kTile;
+          for (int t = 0; t < n_tiles; ++t) {
+            if (c + s_tile[t] > target) {
+              s_tile_hit = t;
+              break;
+            }
+            c += s_tile[t];
+          }
+        }
+        s_target = target;
+        s_before = c;  // the total before the tile
       }
     }
     __syncthreads();
@@ -285,13 +335,14 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
       // Repeat the tile's scan; the lane whose span holds the target walks its elements
       // (its last element with weight when rounding leaves the target past them).
       float w[kLaneElems];
-      const int x0 = s_tile_hit * kTile + lane * kLaneElems;
+      const int x0 = xb + s_tile_hit * kTile + lane * kLaneElems;
       const bool vec = ((reinterpret_cast<uintptr_t>(pu) | reinterpret_cast<uintptr_t>(qu)) & 15) == 0;
-      const float ls = lane_weights(pu, qu, x0, V, vec, s_Sf, k, from_p, false, w);
+      const float ls = lane_weights(pu, qu, x0, xe, vec, s_Sf, k, from_p, false, w);
       const float inc = warp_inclusive_scan(ls);
-      const double hi = s_total + (double)inc;
+      const double target = s_target;
+      const double hi = s_before + (double)inc;
       const double up = __shfl_up_sync(0xffffffffu, hi, 1);
-      const double lo = lane == 0 ? s_total : up;  // the spans tile [before, before + tile)
+      const double lo = lane == 0 ? s_before : up;  // the spans tile [before, before + tile)
       if (ls > 0.f && lo <= target && target < hi) {
         double c = lo;
         int pick = -1;
@@ -305,15 +356,20 @@ __global__ void __launch_bounds__(kThreads, 1) spec_verify_tree_kernel(const Arg
       }
     }
     __syncthreads();
-    if (tid == 0) {
+    if (tid == 0) s_pub_last[pp] = s_found;  // this CTA's find, for the cluster
+    cluster.sync();
+    if (rank == 0 && tid == 0) {
+      int found = -1;
+      for (int r = 0; r < C; ++r) found = max(found, *cluster.map_shared_rank(&s_pub_last[pp], r));
       // Rounding can leave the target at or past the last crossing: the last token with
       // mass, as for the plain rule.
-      const int drawn = total > 0.0 ? (s_found >= 0 ? s_found : s_last) : -1;
+      const int drawn = total > 0.0 ? (found >= 0 ? found : last) : -1;
       out[depth] = drawn;
       a.accepted_len[b] = depth;
       if (drawn < 0) atomicOr(a.err, VAS_DEV_EMPTY_ROW);
       if (fallback) atomicOr(a.err, VAS_DEV_RESIDUAL_FALLBACK);
     }
+    cluster.sync();  // no CTA leaves while a peer may still read its shared memory
     return;
   }
 }
@@ -331,7 +387,8 @@ extern "C" int spec_verify_tree(const float* p, const float* q, const int32_t* d
   if (!p || !q || !draft_tokens || !parents || !accepted_len || !out_tokens || !path)
     return VAS_E_INVALID_ARG;
   if ((int64_t)(n + 1) * V > INT32_MAX / 2) return VAS_E_INVALID_ARG;
-  if ((int64_t)V > (int64_t)kMaxTiles * kTile) return VAS_E_UNSUPPORTED;
+  if ((int64_t)V > kMaxVocab) return VAS_E_UNSUPPORTED;
+  if ((int64_t)B * kMaxCluster > INT32_MAX) return VAS_E_INVALID_ARG;
   int32_t* err = vas::device_error_word();
   if (!err) return VAS_E_CUDA;
   Args a;
@@ -345,18 +402,34 @@ extern "C" int spec_verify_tree(const float* p, const float* q, const int32_t* d
   a.B = B;
   a.n = n;
   a.V = V;
+  // Cluster size and slices as for spec_verify: slices of at least kSliceMin elements,
+  // whole tiles.
+  // Each sequence's walk is long-lived: with many sequences, fewer CTAs per sequence
+  // keep the whole grid resident (two CTAs per SM).
+  int C = (V + kSliceMin - 1) / kSliceMin;
+  if (C > kMaxCluster) C = kMaxCluster;
+  const int sms = vas::num_sms();
+  while (C > 1 && (int64_t)B * C > 2LL * (sms > 0 ? sms : 148)) --C;
+  int slice = (V + C - 1) / C;
+  slice = (slice + kTile - 1) / kTile * kTile;
+  C = (V + slice - 1) / slice;
+  a.slice = slice;
   a.key0 = static_cast<uint32_t>(seed);
   a.key1 = static_cast<uint32_t>(seed >> 32);
   a.err = err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)B);
+  cfg.gridDim = dim3((unsigned)(B * C));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, spec_verify_tree_kernel, a) != cudaSuccess) {
     cudaGetLastError();
     return VAS_E_CUDA;
