@@ -1389,12 +1389,14 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
             tc_fence_after();
             const uint32_t k_lo = umma_desc_lo(smem_u32(stages + slot_s * S::kStageBytes), 16);
             const uint32_t dt = tmem + kTmemS + ((wc + j) & 1) * 32;
-            const int pg = it.page_begin + j * PPS;
-            const int n_in = min(PPS, it.page_end - pg);
+            // Straight-line issue (a branch between products costs more than a product):
+            // every page of the slot, loaded or not -- scores of tokens past the loaded
+            // ones are masked by the consumers.
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
               const uint32_t qstep = ((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4;
-              for (int e = 0; e < n_in; ++e) {
+#pragma unroll
+              for (int e = 0; e < PPS; ++e) {
                 const uint32_t kstep = (e * kPageBytes + (ks >> 2) * (P * 128) + (ks & 3) * 32) >> 4;
                 umma_bf16_lh(dt + e * P, q_lo + qstep, k_lo + kstep, kDescHi, kIdS, ks > 0);
               }
@@ -1424,13 +1426,16 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
               const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
               const uint32_t v_lo = umma_desc_lo(
                   smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
-              for (int kk = 0; kk < loaded / 16; ++kk)
-                umma_bf16_lh(tmem + kTmemO, pb_lo + ((kk * 32) >> 4),
-                             v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO, j > 0 || kk > 0);
-              if constexpr (decltype(prec)::value)
-                for (int kk = 0; kk < loaded / 16; ++kk)
-                  umma_bf16_lh(tmem + kTmemO, pb_lo + kPLoDesc + ((kk * 32) >> 4),
-                               v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO, true);
+              // 16 or 32 loaded tokens (a 32-token page is always whole): the second
+              // 16-token product only when its V rows were loaded.
+              const bool two = P == 32 || loaded > 16;
+              constexpr uint32_t kV1 = tok_off<D, P>(16) >> 4;
+              umma_bf16_lh(tmem + kTmemO, pb_lo, v_lo, kDescHi, kIdO, j > 0);
+              if (two) umma_bf16_lh(tmem + kTmemO, pb_lo + 2, v_lo + kV1, kDescHi, kIdO, true);
+              if constexpr (decltype(prec)::value) {
+                umma_bf16_lh(tmem + kTmemO, pb_lo + kPLoDesc, v_lo, kDescHi, kIdO, true);
+                if (two) umma_bf16_lh(tmem + kTmemO, pb_lo + kPLoDesc + 2, v_lo + kV1, kDescHi, kIdO, true);
+              }
               umma_commit(&empty[slot_s]);
               umma_commit(&bo[b]);
             }
@@ -1457,20 +1462,24 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         if (lane == 0) {
           tc_fence_after();
           const uint32_t pb_lo = p_lo + ((b * S::kPTileBytes) >> 4);
-          for (int h = 0; h < 2 && 2 * j + h < n_stages; ++h) {
+          // Straight-line issue per stage: 16 or 32 loaded tokens (a 32-token page is
+          // always whole).  V (MN-major): 64-column blocks a page half apart, 8-token
+          // groups 1024 B.
+          constexpr uint32_t kV1 = tok_off<D, P>(16) >> 4;
+          auto stage_pv = [&](int h, bool first) {
             const uint32_t st = stage_it + 2 * j + h;
             const int slot_s = st % kSlots;
             const int pg = it.page_begin + (2 * j + h) * PPS;
-            const int loaded = min(PPS, it.page_end - pg) * P;
-            // V (MN-major): 64-column blocks a page half apart, 8-token groups 1024 B.
+            const bool two = P == 32 || min(PPS, it.page_end - pg) * P > 16;
             const uint32_t v_lo = umma_desc_lo(
                 smem_u32(stages + slot_s * S::kStageBytes + S::kOperandBytes), P * 128);
-            for (int kk = 0; kk < loaded / 16; ++kk)
-              umma_bf16_lh(tmem + kTmemO, pb_lo + ((h * 64 + kk * 32) >> 4),
-                           v_lo + (tok_off<D, P>(16 * kk) >> 4), kDescHi, kIdO,
-                           j > 0 || h > 0 || kk > 0);
+            const uint32_t pa = pb_lo + ((h * 64) >> 4);
+            umma_bf16_lh(tmem + kTmemO, pa, v_lo, kDescHi, kIdO, !first);
+            if (two) umma_bf16_lh(tmem + kTmemO, pa + 2, v_lo + kV1, kDescHi, kIdO, true);
             umma_commit(&empty[slot_s]);
-          }
+          };
+          stage_pv(0, j == 0);
+          if (2 * j + 1 < n_stages) stage_pv(1, false);
           umma_commit(&bo[b]);
         }
         __syncwarp();
