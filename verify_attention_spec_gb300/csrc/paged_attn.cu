@@ -1381,39 +1381,51 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
           break;
         }
         ++wq;
-        auto issue_s = [&](int j) -> bool {
-          const uint32_t st = stage_it + j;
-          const int slot_s = st % kSlots;
-          if (!mbar_wait(&stage_ready[slot_s], (st / kSlots) & 1)) return false;
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t k_lo = umma_desc_lo(smem_u32(stages + slot_s * S::kStageBytes), 16);
-            const uint32_t dt = tmem + kTmemS + ((wc + j) & 1) * 32;
-            // Straight-line issue (a branch between products costs more than a product):
-            // every page of the slot, loaded or not -- scores of tokens past the loaded
-            // ones are masked by the consumers.
+        // S_j = Q K_j^T into S buffer (wc + j) & 1, issued by lane 0 once stage j has landed.
+        auto s_products = [&](int j) {
+          const int slot_s = (stage_it + j) % kSlots;
+          const uint32_t k_lo = umma_desc_lo(smem_u32(stages + slot_s * S::kStageBytes), 16);
+          const uint32_t dt = tmem + kTmemS + ((wc + j) & 1) * 32;
+          // Straight-line issue (a branch between products costs more than a product):
+          // every page of the slot, loaded or not -- scores of tokens past the loaded
+          // ones are masked by the consumers.
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-              const uint32_t qstep = ((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4;
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t qstep = ((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4;
 #pragma unroll
-              for (int e = 0; e < PPS; ++e) {
-                const uint32_t kstep = (e * kPageBytes + (ks >> 2) * (P * 128) + (ks & 3) * 32) >> 4;
-                umma_bf16_lh(dt + e * P, q_lo + qstep, k_lo + kstep, kDescHi, kIdS, ks > 0);
-              }
+            for (int e = 0; e < PPS; ++e) {
+              const uint32_t kstep = (e * kPageBytes + (ks >> 2) * (P * 128) + (ks & 3) * 32) >> 4;
+              umma_bf16_lh(dt + e * P, q_lo + qstep, k_lo + kstep, kDescHi, kIdS, ks > 0);
             }
-            umma_commit(&bs[(wc + j) & 1]);
           }
-          __syncwarp();
-          return true;
+          umma_commit(&bs[(wc + j) & 1]);
+        };
+        auto stage_landed = [&](int j) {
+          const uint32_t st = stage_it + j;
+          return mbar_wait(&stage_ready[st % kSlots], (st / kSlots) & 1);
         };
         // The stage loop comes in two copies: a precise unit adds O += P_lo V after each
         // O += P V (this loop is the issue-bound part of prompt chunks, and a branch in
-        // it costs them).
+        // it costs them).  Per stage j: both barriers (P_j written, stage j + 2 landed)
+        // are probed first, so that their latencies overlap, then one straight-line
+        // issue of O += P_j V_j and S_{j+2}.
         auto stages_pv = [&](auto prec) {
-          bool good = issue_s(0) && (n_stages < 2 || issue_s(1));
+          bool good = stage_landed(0) && (n_stages < 2 || stage_landed(1));
+          if (good && lane == 0) {
+            tc_fence_after();
+            s_products(0);
+            if (n_stages > 1) s_products(1);
+          }
+          __syncwarp();
           for (int j = 0; good && j < n_stages; ++j) {
             const uint32_t k = wk + j, b = k & 1;
-            if (!mbar_wait(&bp[b], (k >> 1) & 1)) {
+            const bool more = j + 2 < n_stages;
+            const uint32_t st2 = stage_it + j + 2;
+            bool gp = mbar_test_wait(&bp[b], (k >> 1) & 1);
+            bool g2 = !more || mbar_test_wait(&stage_ready[st2 % kSlots], (st2 / kSlots) & 1);
+            if (!gp) gp = mbar_wait(&bp[b], (k >> 1) & 1);
+            if (!g2) g2 = stage_landed(j + 2);
+            if (!gp || !g2) {
               good = false;
               break;
             }
@@ -1438,9 +1450,11 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
               }
               umma_commit(&empty[slot_s]);
               umma_commit(&bo[b]);
+              // S of stage j + 2 after O of stage j: its completion also covers that
+              // product, the last reader of the P tile stage j + 2 rewrites.
+              if (more) s_products(j + 2);
             }
             __syncwarp();
-            if (j + 2 < n_stages) good = issue_s(j + 2);
           }
           return good;
         };
