@@ -95,6 +95,7 @@ constexpr int kUnitsPerSm = 16;    // split target: work units per SM
 constexpr int kPreciseTokens = 64;
 constexpr int32_t kItemPrecise = 1 << 30;
 constexpr int kPlanThreads = 256;
+constexpr int kOrderBuckets = 64;  // page-count classes of the work order
 constexpr int kPlanSmemSeqs = 4096;
 constexpr int kSeqInvalid = 1;
 
@@ -129,7 +130,7 @@ struct RingEntry {
 };
 
 struct Layout {
-  size_t seqplan, token_seq, items, counters, part_lse, part_o, total;
+  size_t seqplan, token_seq, items, order, counters, part_lse, part_o, total;
   int64_t items_cap, partial_cap;
 };
 
@@ -144,6 +145,7 @@ struct PlanArgs {
   SeqPlan* seqplan;
   int32_t* token_seq;
   Item* items;
+  int32_t* order;  // work order: item indices, longest first
   PlanHeader* header;
   int32_t* counters;
   void* out;
@@ -380,6 +382,34 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
 #pragma unroll
     for (int k = 0; k < 3; ++k) carry[k] += t[k];
   }
+  // Work order: the items by decreasing page count (kOrderBuckets buckets up to the
+  // split length), so that the longest units start first and the grid ends on short
+  // ones (a unit's place in the order changes only which CTA runs it and when).
+  {
+    __shared__ int32_t hist[kOrderBuckets];
+    const int64_t n_items = carry[1] < a.items_cap ? carry[1] : a.items_cap;
+    const int64_t span = c < (int64_t)a.maxp ? c : (int64_t)a.maxp;
+    auto bucket = [&](int64_t i) {
+      const Item& t = a.items[i];
+      const int64_t b = (int64_t)(t.page_end - t.page_begin) * kOrderBuckets / (span + 1);
+      return (int)(b < 0 ? 0 : (b < kOrderBuckets ? b : kOrderBuckets - 1));
+    };
+    for (int b = tid; b < kOrderBuckets; b += kPlanThreads) hist[b] = 0;
+    __syncthreads();  // every item is written, the histogram is clear
+    for (int64_t i = tid; i < n_items; i += kPlanThreads) atomicAdd(&hist[bucket(i)], 1);
+    __syncthreads();
+    if (tid == 0) {
+      int32_t run = 0;
+      for (int b = kOrderBuckets - 1; b >= 0; --b) {
+        const int32_t h = hist[b];
+        hist[b] = run;
+        run += h;
+      }
+    }
+    __syncthreads();
+    for (int64_t i = tid; i < n_items; i += kPlanThreads)
+      a.order[atomicAdd(&hist[bucket(i)], 1)] = (int32_t)i;
+  }
   if (tid == 0) {
     a.header->n_items = (int32_t)(carry[1] < a.items_cap ? carry[1] : a.items_cap);
     a.header->work_counter = 0;
@@ -417,6 +447,7 @@ struct AttnArgs {
   const int32_t* block_table;
   const SeqPlan* seqplan;
   const Item* items;
+  const int32_t* order;  // work order: item indices, longest first
   PlanHeader* header;
   int32_t* counters;
   float* part_o;
@@ -1089,11 +1120,11 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
     Item it{}, it1{};
     SeqPlan sp{}, sp1{};
     if (u < n_units) {
-      it = a.items[u / a.Hkv];
+      it = a.items[a.order[u / a.Hkv]];
       if (it.seq >= 0) sp = a.seqplan[it.seq];
     }
     if (u1 < n_units) {
-      it1 = a.items[u1 / a.Hkv];
+      it1 = a.items[a.order[u1 / a.Hkv]];
       if (it1.seq >= 0) sp1 = a.seqplan[it1.seq];
     }
     if (lane == 0) u2_lane0 = atomicAdd(work_counter, 1);
@@ -1129,7 +1160,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
       const int32_t u2 = __shfl_sync(0xffffffffu, u2_lane0, 0);
       Item it2{};
       SeqPlan sp2{};
-      if (u2 < n_units) it2 = a.items[u2 / a.Hkv];
+      if (u2 < n_units) it2 = a.items[a.order[u2 / a.Hkv]];
       if (lane == 0) u2_lane0 = atomicAdd(work_counter, 1);
 
       if (it.seq >= 0) {
@@ -2137,7 +2168,7 @@ __global__ void __launch_bounds__(128) attn_f32_kernel(const AttnArgs a) {
   pdl_wait_prior_grid();
   const int32_t n_units = a.header->n_items * a.Hkv;
   for (int32_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const Item it = a.items[u / a.Hkv];
+    const Item it = a.items[a.order[u / a.Hkv]];
     if (it.seq < 0) continue;
     const int head = u % a.Hkv;
     const SeqPlan sp = a.seqplan[it.seq];
@@ -2257,6 +2288,8 @@ Layout make_layout(const vas_attn_dims* d, int64_t items_cap, int64_t partial_ca
   off = align_up(off + (size_t)d->total_q_tokens * 4, 256);
   L.items = off;
   off = align_up(off + (size_t)items_cap * sizeof(Item), 256);
+  L.order = off;
+  off = align_up(off + (size_t)items_cap * 4, 256);
   L.counters = off;
   off = align_up(off + (size_t)items_cap * d->num_kv_heads * 4, 256);
   L.part_lse = off;
@@ -2433,6 +2466,7 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
   pa.seqplan = reinterpret_cast<SeqPlan*>(ws + lay.seqplan);
   pa.token_seq = reinterpret_cast<int32_t*>(ws + lay.token_seq);
   pa.items = reinterpret_cast<Item*>(ws + lay.items);
+  pa.order = reinterpret_cast<int32_t*>(ws + lay.order);
   pa.header = reinterpret_cast<PlanHeader*>(ws);
   pa.counters = reinterpret_cast<int32_t*>(ws + lay.counters);
   pa.out = out;
@@ -2480,6 +2514,7 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
   aa.block_table = block_table;
   aa.seqplan = pa.seqplan;
   aa.items = pa.items;
+  aa.order = pa.order;
   aa.header = pa.header;
   aa.counters = pa.counters;
   aa.part_o = reinterpret_cast<float*>(ws + lay.part_o);
