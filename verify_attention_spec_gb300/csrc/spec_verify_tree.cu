@@ -10,6 +10,10 @@
 //   max(0, R - S q_u) and S into its sum.  An accepted child becomes u.  When a node's
 //   children are all rejected, or it has none, one token is drawn from R by inverse CDF
 //   and the walk ends.  A zero residual after a rejection draws from p_u instead.
+// With q_u >= 0 and every S >= 0 the residual after k rejections has a closed form,
+// R_k = max(0, p_u - c_k q_u) with c_k = S_0 + ... + S_{k-1} (by induction: where
+// R_{k-1} = 0, p_u <= c_{k-1} q_u <= c_k q_u), so each element costs one product and
+// one maximum in any pass.
 // For a chain this is spec_verify's rule with its uniforms: r_c is word 0 of
 // Philox(c - 1, b), the draw at node u uses word 1 of Philox(u, b).
 //
@@ -22,9 +26,8 @@
 // in fp64 to the slice total, published to the cluster, and every CTA adds the C slice
 // totals in rank order.  A draw finds the slice, then the tile where the inverse CDF
 // crosses its target; that CTA repeats the tile's scan and walks the crossing lane's 8
-// elements.  Weights are fp32 (R_k recomputed per element from p, q and S_0..S_{k-1});
-// totals and thresholds are fp64 (this part's fp64 rate is too low for fp64 per
-// element).
+// elements.  Weights are fp32 (R_k from p, q and c_k); totals, c_k and thresholds are
+// fp64 (this part's fp64 rate is too low for fp64 per element).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -57,19 +60,11 @@ struct Args {
   int32_t* err;
 };
 
-// R_k(y): R_0 = p, R_{i+1} = max(0, R_i - S_i q), with S_0 = 1 (fp32 per element).
-__device__ __forceinline__ float residual(float p, float q, const float* S, int k) {
-  float r = p;
-  for (int i = 0; i < k; ++i) r = fmaxf(r - S[i] * q, 0.f);
-  return r;
-}
-
-// The weight of element y in a pass: the rejection's new residual (next = true), or
-// the row to draw from (p_u, or R_k).
-__device__ __forceinline__ float weight(float p, float q, const float* S, int k, bool from_p,
-                                        bool next) {
-  if (next) return fmaxf(residual(p, q, S, k) - S[k] * q, 0.f);
-  return from_p ? p : residual(p, q, S, k);
+// The weight of element y in a pass: max(0, p - c q), the residual for the pass's
+// c (c_{k+1} for a rejection's new residual, c_k for a draw from R_k); a draw from p_u
+// passes c = 0.
+__device__ __forceinline__ float weight(float p, float q, float c) {
+  return fmaxf(fmaf(-c, q, p), 0.f);
 }
 
 constexpr int kLaneElems = 8;
@@ -104,14 +99,13 @@ __device__ __forceinline__ void lane_load(const float* pu, const float* qu, int 
 
 // One lane's 8 weights from x0 (past V: zero), and their fp32 sum.
 __device__ __forceinline__ float lane_weights(const float* pu, const float* qu, int x0, int V,
-                                              bool vec, const float* S, int k, bool from_p,
-                                              bool next, float (&w)[kLaneElems]) {
+                                              bool vec, float c, float (&w)[kLaneElems]) {
   float p8[kLaneElems], q8[kLaneElems];
   lane_load(pu, qu, x0, V, vec, p8, q8);
   float sum = 0.f;
 #pragma unroll
   for (int e = 0; e < kLaneElems; ++e) {
-    w[e] = x0 + e < V ? weight(p8[e], q8[e], S, k, from_p, next) : 0.f;
+    w[e] = x0 + e < V ? weight(p8[e], q8[e], c) : 0.f;
     sum += w[e];
   }
   return sum;
@@ -132,9 +126,8 @@ __device__ __forceinline__ float warp_inclusive_scan(float v) {
 // A pass over this CTA's slice [xb, V' = min(V, xb + slice)): every tile's total into
 // s_tile[]; returns the slice total (every thread) and leaves the slice's last element
 // with positive weight in *s_last.
-__device__ double pass_totals(const float* pu, const float* qu, int xb, int V, const float* S,
-                              int k, bool from_p, bool next, double* s_tile, int* s_last,
-                              double* s_total) {
+__device__ double pass_totals(const float* pu, const float* qu, int xb, int V, float c,
+                              double* s_tile, int* s_last, double* s_total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n_tiles = (V - xb + kTile - 1) / kTile;
   const bool vec = ((reinterpret_cast<uintptr_t>(pu) | reinterpret_cast<uintptr_t>(qu)) & 15) == 0;
@@ -158,7 +151,7 @@ __device__ double pass_totals(const float* pu, const float* qu, int xb, int V, c
       if (t0 + j < n_tiles)
 #pragma unroll
         for (int e = 0; e < kLaneElems; ++e) {
-          const float w = x0 + e < V ? weight(p8[j][e], q8[j][e], S, k, from_p, next) : 0.f;
+          const float w = x0 + e < V ? weight(p8[j][e], q8[j][e], c) : 0.f;
           v[j] += w;
           if (w > 0.f) last = x0 + e;
         }
@@ -191,8 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
   const int n = a.n, V = a.V;
   const int xb = min(V, rank * a.slice), xe = min(V, xb + a.slice);  // this CTA's slice
   __shared__ int32_t s_par[kMaxNodes], s_x[kMaxNodes];
-  __shared__ double s_S[kMaxNodes + 1];
-  __shared__ float s_Sf[kMaxNodes + 1];
+  __shared__ double s_S[kMaxNodes + 1];  // S_0 .. S_k of the current node
   __shared__ double s_tile[kMaxTiles];
   __shared__ double s_total, s_pub[2];   // slice total; published, by pass parity
   __shared__ int32_t s_last, s_pub_last[2];
@@ -228,10 +220,8 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
   int pp = 0;  // publication slot: passes alternate, one cluster barrier each
   // A pass over the slices; returns the row total, identical in every CTA (slice
   // totals added in rank order), and the row's last element with weight in *last.
-  auto cluster_pass = [&](const float* pu, const float* qu, int k, bool from_p, bool next,
-                          int* last) -> double {
-    const double mine = pass_totals(pu, qu, xb, xe, s_Sf, k, from_p, next, s_tile, &s_last,
-                                    &s_total);
+  auto cluster_pass = [&](const float* pu, const float* qu, float c, int* last) -> double {
+    const double mine = pass_totals(pu, qu, xb, xe, c, s_tile, &s_last, &s_total);
     if (tid == 0) {
       s_pub[pp] = mine;
       s_pub_last[pp] = s_last;
@@ -254,16 +244,14 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
     const float* qu = a.q + ((size_t)b * n + (u < n ? u : 0)) * V;
     int k = 0, next = -1, last = -1;
     bool fallback = false;
-    if (tid == 0) {
-      s_S[0] = 1.0;
-      s_Sf[0] = 1.f;
-    }
+    double ck = 0.0;  // c_k = S_0 + ... + S_{k-1} (every thread keeps the same sum)
+    if (tid == 0) s_S[0] = 1.0;
     for (int c = u + 1; c <= n; ++c) {
       if (s_par[c - 1] != u) continue;
       if (tid == 0) {
         const int x = s_x[c - 1];
         const float qx = qu[x];
-        const double rx = residual(pu[x], qx, s_Sf, k);
+        const double rx = fmax((double)pu[x] - ck * (double)qx, 0.0);
         const uint4 w = philox4x32_10(make_uint4((uint32_t)(c - 1), (uint32_t)b, 0u, 0u),
                                       a.key0, a.key1);
         s_accept = philox_uniform(w.x) * s_S[k] * (double)qx <= rx;
@@ -276,12 +264,10 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
         break;
       }
       // Rejected: the new residual's total.
-      const double total = cluster_pass(pu, qu, k, false, true, &last);
+      ck += s_S[k];
+      const double total = cluster_pass(pu, qu, (float)ck, &last);
       ++k;
-      if (tid == 0) {
-        s_S[k] = total;
-        s_Sf[k] = (float)total;
-      }
+      if (tid == 0) s_S[k] = total;
       __syncthreads();
       if (total == 0.0) {
         fallback = true;
@@ -299,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
     }
     // Draw at node u: from R_k, or from p_u (nothing rejected, or the fallback).
     const bool from_p = k == 0 || fallback;
-    const double total = cluster_pass(pu, qu, k, from_p, false, &last);
+    const double total = cluster_pass(pu, qu, from_p ? 0.f : (float)ck, &last);
     if (tid == 0) {
       s_tile_hit = -1;
       s_found = -1;
@@ -337,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Arg
       float w[kLaneElems];
       const int x0 = xb + s_tile_hit * kTile + lane * kLaneElems;
       const bool vec = ((reinterpret_cast<uintptr_t>(pu) | reinterpret_cast<uintptr_t>(qu)) & 15) == 0;
-      const float ls = lane_weights(pu, qu, x0, xe, vec, s_Sf, k, from_p, false, w);
+      const float ls = lane_weights(pu, qu, x0, xe, vec, from_p ? 0.f : (float)ck, w);
       const float inc = warp_inclusive_scan(ls);
       const double target = s_target;
       const double hi = s_before + (double)inc;
