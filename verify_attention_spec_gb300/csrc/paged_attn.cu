@@ -85,7 +85,9 @@ __host__ __device__ __forceinline__ int row_block(int R) {
 constexpr int kNarrowRows = 16;    // units with at most this many rows take the K Q^T form
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
-constexpr int kUnitsPerSm = 16;    // split target: work units per SM
+constexpr int kUnitsPerSm = 16;    // work-list room per SM in the recommended workspace
+constexpr int kSplitTargetPerSm = 8;  // split target: work units per SM (the longest-first
+                                      // order keeps the tail short with units this long)
 // Row blocks in which some row sees fewer KV positions than this are "precise": with
 // few tokens each softmax weight is large, and one bf16 rounding of P (relative 2^-8)
 // would show in the output at the 1e-2 level.  The plan marks their items with
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   const bool lengths_ok = rows == a.T && bad == 0;
   if (tid == 0 && !lengths_ok) atomicOr(a.err, VAS_DEV_BAD_LENGTHS);
 
-  // Split length: about kUnitsPerSm units per SM, at least min_chunk pages, a whole
+  // Split length: about kSplitTargetPerSm units per SM, at least min_chunk pages, a whole
   // number of stages; doubled until the work list and the partials fit the workspace.
   int64_t c;
   if (a.no_split) {
@@ -2484,7 +2486,7 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
   // staging, the partial written and merged) than it returns in balance across SMs.
   pa.min_chunk = 32 * pa.pps;
   pa.no_split = bf16 ? 0 : 1;
-  pa.target_units = kUnitsPerSm * sms;
+  pa.target_units = kSplitTargetPerSm * sms;
   pa.is_bf16 = bf16 ? 1 : 0;
   pa.tree_mask = tree_mask;
   pa.items_cap = lay.items_cap;
