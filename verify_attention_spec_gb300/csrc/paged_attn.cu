@@ -86,7 +86,7 @@ constexpr int kNarrowRows = 16;    // units with at most this many rows take the
 constexpr int kRing = 4;           // unit descriptors the producer may run ahead
 constexpr int kRbBits = 12;        // row-block index bits in Item::split_rb
 constexpr int kUnitsPerSm = 16;    // work-list room per SM in the recommended workspace
-constexpr int kSplitTargetPerSm = 8;  // split target: work units per SM (the longest-first
+constexpr int kSplitTargetPerSm = 4;  // split target: work units per SM (the longest-first
                                       // order keeps the tail short with units this long)
 // Row blocks in which some row sees fewer KV positions than this are "precise": with
 // few tokens each softmax weight is large, and one bf16 rounding of P (relative 2^-8)
