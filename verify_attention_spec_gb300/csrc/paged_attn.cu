@@ -179,6 +179,14 @@ __device__ __forceinline__ int32_t splits_for(const SeqShape& s, int64_t chunk) 
   return (int32_t)((s.npages + chunk - 1) / chunk);
 }
 
+// A sequence's split length: the call's c, at least twice the minimum for sequences
+// whose units take the narrow path (at most kNarrowRows rows per KV head).  A narrow
+// unit's fixed costs (query staging, the merge of its warps, the split's partial) weigh
+// more against its short per-stage time than a wide unit's do.
+__device__ __forceinline__ int64_t seq_chunk(const PlanArgs& a, const SeqShape& s, int64_t c) {
+  return s.R <= kNarrowRows && c < 2 * (int64_t)a.min_chunk ? 2 * (int64_t)a.min_chunk : c;
+}
+
 // Block-wide sums of N counters at once.
 template <int N>
 __device__ __forceinline__ void block_sum(int64_t (&v)[N], int64_t (*red)[4]) {
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     int64_t v[2] = {0, 0};  // items, partial rows
     for (int i = tid; i < a.B; i += kPlanThreads) {
       const SeqShape s = shape(i);
-      const int32_t ns = splits_for(s, c);
+      const int32_t ns = splits_for(s, seq_chunk(a, s, c));
       v[0] += (int64_t)ns * s.nrb;
       if (ns > 1) v[1] += (int64_t)ns * a.Hkv * s.R;
     }
@@ -333,7 +341,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     if (i < a.B) {
       s = shape(i);
       qrows = s.ql > 0 ? s.ql : 0;
-      ns = splits_for(s, c);
+      ns = splits_for(s, seq_chunk(a, s, c));
     }
     int64_t v[3] = {qrows, (int64_t)ns * s.nrb, ns > 1 ? (int64_t)ns * a.Hkv * s.R : 0};
     int64_t t[3];
@@ -365,8 +373,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
         // tree masks of a skipped sequence's rows may not exist (rows past T).
         int64_t it = my_item0;
         for (int sp_i = 0; sp_i < ns; ++sp_i) {
-          const int32_t pb = (int32_t)(sp_i * c);
-          const int32_t pe = (int32_t)((sp_i + 1) * c < s.npages ? (sp_i + 1) * c : s.npages);
+          const int64_t cs = seq_chunk(a, s, c);
+          const int32_t pb = (int32_t)(sp_i * cs);
+          const int32_t pe = (int32_t)((sp_i + 1) * cs < s.npages ? (sp_i + 1) * cs : s.npages);
           for (int rb = 0; rb < s.nrb && it < a.items_cap; ++rb) {
             const bool prec = a.is_bf16 && sp.nsplit > 0 && rb_precise(a, s, my_row0, rb);
             Item item;
@@ -390,7 +399,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
   {
     __shared__ int32_t hist[kOrderBuckets];
     const int64_t n_items = carry[1] < a.items_cap ? carry[1] : a.items_cap;
-    const int64_t span = c < (int64_t)a.maxp ? c : (int64_t)a.maxp;
+    const int64_t cmax = c > 2 * (int64_t)a.min_chunk ? c : 2 * (int64_t)a.min_chunk;
+    const int64_t span = cmax < (int64_t)a.maxp ? cmax : (int64_t)a.maxp;  // longest item
     auto bucket = [&](int64_t i) {
       const Item& t = a.items[i];
       const int64_t b = (int64_t)(t.page_end - t.page_begin) * kOrderBuckets / (span + 1);
