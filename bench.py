@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--workload", default="stress70b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-call timing of the small batches")
+    ap.add_argument("--config-reps", type=int, default=200)
     ap.add_argument("--max-seqs", type=int, default=0,
                     help="profiling only: keep the first N sequences of the workload")
     return ap.parse_args()
@@ -116,6 +119,20 @@ def elem_sizes(kv_dtype):
     if kv_dtype in wl.QUANTIZED:
         return 2, 1
     return (2, 2) if kv_dtype == wl.BF16 else (4, 4)
+
+
+def acceptance_stats(accepted_len, k, p=None, q=None):
+    """Per-token acceptance of the drafts: accepted / ratio tests run (a sequence that
+    accepts a drafts ran min(a + 1, k) tests), and, given the rows, the expected rate
+    alpha = mean over (sequence, position) of sum_x min(p_i(x), q_i(x))."""
+    acc = np.asarray(accepted_len, dtype=np.int64)
+    tests = np.minimum(acc + 1, k)
+    out = {"mean_accepted": float(acc.mean()),
+           "per_token_acceptance": float(acc.sum() / max(int(tests.sum()), 1))}
+    if p is not None and q is not None and k > 0:
+        out["alpha_sum_min_pq"] = float(np.mean([np.minimum(p[b, :k], q[b]).sum(-1).mean()
+                                                 for b in range(p.shape[0])]))
+    return out
 
 
 def tree_verify_bytes(accepted_len, path, parents, V):
@@ -199,22 +216,28 @@ class ClockSampler:
 # ncu evidence (committed summary): DRAM traffic per launch of the attention kernel,
 # valid only while the kernel source is unchanged.
 # ---------------------------------------------------------------------------------
-def kernel_source_hash():
+KERNEL_SOURCES = {"paged_attn": ["paged_attn.cu", "device_util.cuh"],
+                  "spec_verify": ["spec_verify.cu", "device_util.cuh", "philox.cuh"]}
+
+
+def kernel_source_hash(kernel="paged_attn"):
     h = hashlib.sha256()
-    for f in ["paged_attn.cu", "device_util.cuh"]:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "verify_attention_spec_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload):
-    path = os.path.join(ROOT, "profiles", f"paged_attn_{workload}_ncu.md")
+def ncu_traffic(workload, kernel="paged_attn"):
+    """DRAM bytes per full-size launch of `kernel` on `workload` from its committed ncu
+    summary, or None when there is none or the kernel has changed since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
@@ -320,7 +343,37 @@ def cpu_baseline(a, v, name, parents=None):
         tv = time.perf_counter() - t0
         out["spec_verify_seqs_per_s"] = v.B / tv
         out["sample"] += f"; spec_verify on all {v.B} verify sequences ({tv:.2f} s)"
+    out["single_thread"] = single_thread_oracle()
     return out
+
+
+def single_thread_oracle(names=("tiny", "decode64")):
+    """The oracle on one host thread over the whole of each small batch (GB/s of
+    algorithmic bytes; the tiny case also its spec_verify)."""
+    import oracle
+    from verify_attention_spec_gb300 import workloads as wl
+    n0 = oracle.num_threads()
+    res = {}
+    oracle.set_num_threads(1)
+    try:
+        for nm in names:
+            a = wl.workload_attention(nm)
+            smp = oracle_sample(a, list(range(a.num_seqs)))
+            runs, dt = 0, 0.0
+            while dt < 1.0:
+                dt += time_oracle_attention(smp, a.kv_dtype)
+                runs += 1
+            by = attn_bytes(smp["lens"], smp["qlens"], a.num_q_heads, a.num_kv_heads,
+                            a.head_dim, a.page_size, *elem_sizes(a.kv_dtype)) * runs
+            res[nm] = {"gbs": by / dt / 1e9, "runs": runs, "seconds": dt}
+            v = wl.workload_verify(nm)
+            if v is not None:
+                t0 = time.perf_counter()
+                run_oracle_verify(v)
+                res[nm]["spec_verify_seqs_per_s"] = v.B / (time.perf_counter() - t0)
+    finally:
+        oracle.set_num_threads(n0)
+    return res
 
 
 # ---------------------------------------------------------------------------------
@@ -364,6 +417,95 @@ def whole_job_rate(bytes_per_rank_step, world, ms_per_step):
     """Weak scaling: every rank streams its own batch, so the job moves world times the
     per-rank bytes in the slowest rank's step time (GB/s)."""
     return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
+SMALL_CONFIGS = ["decode64", "verify32", "mixed272"]
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+class L2Flush:
+    """Evicts the L2 between timed reps: writes one buffer larger than L2, then reads
+    another, so that the lines left behind are clean (dirty lines would be written back
+    while the next timed kernel reads)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
+def time_small_config(name, dev, reps, peak):
+    """One of the small batches (0.27-0.45 GB of KV per call, launch- and latency-scale):
+    `reps` calls of paged_attn_fwd then spec_verify, each preceded by a write of a
+    buffer larger than L2 and timed alone with CUDA events on the launching stream.
+    Returns median and best per call, with GB/s and the fraction of `peak` taken from
+    the median."""
+    import torch
+    from verify_attention_spec_gb300 import binding as vas
+    from verify_attention_spec_gb300 import workloads as wl
+    a = wl.workload_attention(name)
+    mv = lambda t: None if t is None else t.to(dev).contiguous()
+    a = wl.AttentionInputs(*(mv(t) for t in (a.q, a.k_pages, a.v_pages, a.block_table,
+                                             a.seq_lens, a.query_lens)),
+                           a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype)
+    v = wl.workload_verify(name)
+    dims = vas.attn_dims(a.q, a.k_pages, a.block_table, a.seq_lens)
+    ws = vas.alloc_workspace(dims, device=dev)
+    out = torch.empty_like(a.q)
+    lse = torch.empty(a.q.shape[0], a.q.shape[1], dtype=torch.float32, device=dev)
+    if v is not None:
+        p_d, q_d, x_d = (torch.from_numpy(x).to(dev) for x in (v.p, v.q, v.draft))
+        acc_d = torch.empty(v.B, dtype=torch.int32, device=dev)
+        tok_d = torch.empty(v.B, v.k + 1, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+
+    def call():
+        vas.paged_attn_fwd(a.q, a.k_pages, a.v_pages, a.block_table, a.seq_lens, a.query_lens,
+                           out, lse, ws, dims=dims)
+
+    def verify():
+        vas.spec_verify(p_d, q_d, x_d, v.seed, acc_d, tok_d)
+
+    for _ in range(5):
+        call()
+        if v is not None:
+            verify()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in ev:
+        flush()
+        e[0].record()
+        call()
+        e[1].record()
+        if v is not None:
+            verify()
+        e[2].record()
+    torch.cuda.synchronize()
+    at = np.array([e[0].elapsed_time(e[1]) for e in ev]) * 1e3
+    by = attn_bytes(a.seq_lens.cpu().numpy(), a.query_lens.cpu().numpy(), a.num_q_heads,
+                    a.num_kv_heads, a.head_dim, a.page_size, *elem_sizes(a.kv_dtype))
+    med = float(np.median(at))
+    res = {"workload": workload_desc(name), "reps": reps,
+           "l2": f"before every rep a {L2_FLUSH_BYTES >> 20} MiB buffer written and another read",
+           "paged_attn": {"us_median": med, "us_best": float(at.min()), "algorithmic_bytes": by,
+                          "gbs": by / (med * 1e-6) / 1e9,
+                          "frac_of_measured_peak": by / (med * 1e-6) / 1e9 / peak,
+                          "frac_of_nominal_8tbs": by / (med * 1e-6) / 1e9 / NOMINAL_HBM_GBS}}
+    if v is not None:
+        vt = np.array([e[1].elapsed_time(e[2]) for e in ev]) * 1e3
+        vb = verify_bytes(acc_d.cpu().numpy(), v.k, v.V)
+        vmed = float(np.median(vt))
+        res["spec_verify"] = {"us_median": vmed, "us_best": float(vt.min()),
+                              "seqs_per_s": v.B / (vmed * 1e-6), "algorithmic_bytes": vb,
+                              "gbs": vb / (vmed * 1e-6) / 1e9,
+                              "frac_of_measured_peak": vb / (vmed * 1e-6) / 1e9 / peak,
+                              **acceptance_stats(acc_d.cpu().numpy(), v.k, v.p, v.q)}
+    del flush
+    return res
 
 
 def run_ours(args):
@@ -615,14 +757,27 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
+    attn_steps = np.array([e[0].elapsed_time(e[1]) for e in ev]) * 1e3
+    res["paged_attn"]["us_median"] = float(np.median(attn_steps))
+    res["paged_attn"]["us_best"] = float(attn_steps.min())
     if v is not None:
         acc = acc_d.cpu().numpy()
+        ver_steps = np.array([e[1].elapsed_time(e[2]) for e in ev]) * 1e3
+        ver_gbs = v_bytes / (ver_ms * 1e-3) / 1e9
         res["spec_verify"] = {"seqs_per_s": v.B / (ver_ms * 1e-3), "ms": ver_ms,
-                              "gbs": v_bytes / (ver_ms * 1e-3) / 1e9, "algorithmic_bytes": v_bytes,
-                              "mean_accepted": float(acc.mean()),
-                              "acceptance_rate": float(acc.mean() / v.k)}
+                              "us_median": float(np.median(ver_steps)),
+                              "us_best": float(ver_steps.min()),
+                              "gbs": ver_gbs, "algorithmic_bytes": v_bytes,
+                              "frac_of_measured_peak": ver_gbs / peak,
+                              "frac_of_nominal_8tbs": ver_gbs / NOMINAL_HBM_GBS,
+                              "traffic": ncu_traffic(name, "spec_verify"),
+                              **(acceptance_stats(acc, v.k, v.p, v.q) if v.parents is None
+                                 else acceptance_stats(acc, v.k))}
     if e2e is not None:
         res["e2e"] = e2e
+    if not args.no_configs and not args.max_seqs and name == "stress70b":
+        res["configs"] = {c: time_small_config(c, dev, max(args.config_reps, 100), peak)
+                          for c in SMALL_CONFIGS}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(a, v, name, attn_parents)
     if rank == 0:

@@ -140,7 +140,8 @@ int paged_attn_fwd(const void* q, const void* k_pages, const void* v_pages,
  * section "4. Tree Attention & Medusa Heads" -- the draft is a tree of candidate
  * tokens, verified in one pass under a tree attention mask; and
  * "llm-inference-optimization-batching" (tempatgunting.com), section "Draft Model
- * Selection and Tree-Style Variants" -- the verification mask becomes a tree mask.
+ * Selection and Tree-Style Variants" -- verifying a tree of drafts masks attention by
+ * the tree's shape.
  *
  * tree_mask   [T] device uint64, 8-byte aligned, one word per query token (the rows of
  *             q).  For query token j of sequence i, bit a (a < j) set means draft token a
@@ -201,8 +202,9 @@ int paged_attn_fwd_quant(const void* q, const void* k_pages, const void* v_pages
  * memory.  The web pages have no counterpart; this is a property of the library.
  * Scratch space is a 32 MiB array in device global memory that the library reserves on
  * every GPU where its device code is loaded, held until the process exits; the call
- * itself allocates nothing.  The first call on a device looks up that array's address;
- * make that first call before any stream capture.  Arguments and results are those of
+ * itself allocates nothing.  The first call on a device looks up that array's address
+ * (and so does the first call after the device's context has been created anew, e.g.
+ * after cudaDeviceReset); make that first call before any stream capture.  Arguments and results are those of
  * paged_attn_fwd.  Returns VAS_E_WORKSPACE when the batch needs more than 32 MiB of plan
  * space (paged_attn_workspace_min(dims) > 32 MiB; thousands of sequences fit); a batch
  * whose split partials would not fit is split less finely instead.  Every call on a

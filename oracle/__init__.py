@@ -80,6 +80,8 @@ def _load():
     lib.oracle_spec_verify_tree.restype = i32
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i32
+    lib.oracle_set_num_threads.argtypes = [i32]
+    lib.oracle_set_num_threads.restype = None
     _lib = lib
     return lib
 
@@ -90,6 +92,11 @@ def _ptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (for timing)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _as_storage(x: np.ndarray, dtype_code: int) -> np.ndarray:

@@ -27,7 +27,7 @@
  *    Random Numbers: As Easy as 1, 2, 3", SC'11 (the published counter-based
  *    generator; the pages only say "random()").
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (the plainest one the rest supports):
  *  - seq_lens[i] counts every KV token of sequence i, including this step's query
  *    tokens; query token j of sequence i sits at absolute position L_i - ql_i + j and
  *    attends to positions 0..that position (causal inside the draft window).
@@ -65,6 +65,16 @@ int oracle_num_threads(void) {
   return omp_get_max_threads();
 #else
   return 1;
+#endif
+}
+
+/* Threads the parallel loops use from now on (timing a single-thread baseline); n < 1
+ * leaves the setting as it is. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
 #endif
 }
 

@@ -69,20 +69,9 @@ def run_gpu_attention_tree(vas, a: wl.AttentionInputs, masks: np.ndarray, worksp
     return run_gpu_attention(vas, a, workspace_bytes=workspace_bytes, tree_masks=masks)
 
 
-def ancestor_masks(parents: np.ndarray, qlens) -> np.ndarray:
-    """The kernel's tree encoding from parent pointers: per query token a uint64 whose bit
-    a is set when token a of its sequence is a proper ancestor of it."""
-    masks = np.zeros(len(parents), dtype=np.uint64)
-    row0 = 0
-    for ql in np.asarray(qlens, dtype=np.int64):
-        for j in range(int(ql)):
-            m, a = 0, int(parents[row0 + j])
-            while a >= 0:
-                m |= 1 << a
-                a = int(parents[row0 + a])
-            masks[row0 + j] = m
-        row0 += int(ql)
-    return masks
+# The kernel's tree encoding (one uint64 of proper ancestors per query token) has a single
+# definition, in the input generator; the tests use that one.
+ancestor_masks = wl.ancestor_bits
 
 
 def oracle_attention(a: wl.AttentionInputs, parents=None):
@@ -121,36 +110,6 @@ def compare_attention(out, lse, ref_out, ref_lse, kv_dtype, rows=None):
     assert rel_l2 <= tol["rel_l2"], f"rel-L2 {rel_l2}"
     assert lse_err <= tol["lse"], f"lse {lse_err}"
     return dict(max_abs=max_abs, rel_l2=rel_l2, lse=lse_err)
-
-
-def subset_inputs(a: wl.AttentionInputs, seqs) -> wl.AttentionInputs:
-    """The chosen sequences only, with their pages copied into a compact pool (the block
-    table is renumbered; paging is invisible to the result).  CPU tensors."""
-    bt = a.block_table.cpu().numpy()
-    lens = a.seq_lens.cpu().numpy()
-    qlens = a.query_lens.cpu().numpy()
-    row0 = np.concatenate([[0], np.cumsum(qlens)])
-    P = a.page_size
-    pages, new_bt, q_rows = [], [], []
-    for i in seqs:
-        n = (lens[i] + P - 1) // P
-        ids = bt[i, :n]
-        base = sum(len(p) for p in pages)
-        pages.append(ids)
-        new_bt.append(np.arange(base, base + n, dtype=np.int32))
-        q_rows.append(np.arange(row0[i], row0[i + 1]))
-    all_ids = torch.from_numpy(np.concatenate(pages).astype(np.int64)).to(a.k_pages.device)
-    maxp = max(len(r) for r in new_bt)
-    btn = np.full((len(seqs), maxp), -1, dtype=np.int32)
-    for r, ids in enumerate(new_bt):
-        btn[r, :len(ids)] = ids
-    rows = torch.from_numpy(np.concatenate(q_rows)).to(a.q.device)
-    sc = lambda t: None if t is None else t[all_ids.to(t.device)].cpu()
-    return wl.AttentionInputs(a.q[rows].cpu(), a.k_pages[all_ids].cpu(), a.v_pages[all_ids].cpu(),
-                              torch.from_numpy(btn), torch.from_numpy(lens[seqs].astype(np.int32)),
-                              torch.from_numpy(qlens[seqs].astype(np.int32)), a.num_q_heads,
-                              a.num_kv_heads, a.head_dim, a.page_size, a.kv_dtype, sc(a.k_scale),
-                              sc(a.v_scale)), np.concatenate(q_rows)
 
 
 def query_slice_inputs(a: wl.AttentionInputs, seq: int, j0: int, n: int):

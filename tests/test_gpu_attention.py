@@ -8,7 +8,7 @@ import oracle
 from verify_attention_spec_gb300 import workloads as wl
 
 from gpu_common import (compare_attention, oracle_attention, query_slice_inputs,
-                        run_gpu_attention, subset_inputs, to_device)
+                        run_gpu_attention, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,26 +22,15 @@ def test_workload_full_parity(vas_lib, name):
     assert vas_lib.vas_last_device_error() == 0
 
 
-def test_stress70b_full_size_sampled(vas_lib):
+def test_stress70b_full_size(vas_lib):
     """The full 70B-shape batch (512 sequences, 64/8 heads, page 32, ~8 GB of KV) in the
-    bench's launch configuration; the oracle checks a sample of sequences one by one:
-    the longest, every sort of verify sequence and a random handful."""
-    a = wl.workload_attention("stress70b", pool_device="cuda")
-    a = to_device(a)
+    bench's launch configuration, every row against the oracle: every work-order
+    position, split count and merge of the headline launch."""
+    a = to_device(wl.workload_attention("stress70b", pool_device="cuda"))
     out, lse = run_gpu_attention(vas_lib, a)
-    lens = a.seq_lens.cpu().numpy()
-    qlens = a.query_lens.cpu().numpy()
-    rng = np.random.default_rng(0)
-    longest = list(np.argsort(lens)[-3:])
-    verify = list(rng.choice(np.nonzero(qlens > 1)[0], 4, replace=False))
-    decode = list(rng.choice(np.nonzero(qlens == 1)[0], 4, replace=False))
-    seqs = sorted(set(int(s) for s in longest + verify + decode))
-    sub, rows = subset_inputs(a, seqs)
-    ref_o, ref_l = oracle_attention(sub)
-    compare_attention(out, lse, ref_o, ref_l, a.kv_dtype, rows=rows)
-    # every row of the full batch is finite
-    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     assert vas_lib.vas_last_device_error() == 0
+    ref_o, ref_l = oracle_attention(a)
+    compare_attention(out, lse, ref_o, ref_l, a.kv_dtype)
 
 
 def _case(lens, qlens, Hq=8, Hkv=2, D=128, P=16, dtype=wl.BF16, seed=3, pool_pages=None):

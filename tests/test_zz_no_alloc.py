@@ -12,7 +12,7 @@ import torch
 
 from verify_attention_spec_gb300 import workloads as wl
 
-from gpu_common import TOL, run_gpu_attention, to_device
+from gpu_common import TOL, compare_attention, oracle_attention, run_gpu_attention, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -32,21 +32,32 @@ def _call_static(vas, a, out, lse):
                            p(a.query_lens), p(out), p(lse), ctypes.byref(dims), stream)
 
 
+STATIC_BYTES = 32 << 20  # the library's fixed scratch array
+
+
 @pytest.mark.parametrize("name", ["verify32", "mixed272"])
 def test_static_workspace_matches_caller_workspace_twice(vas_lib, name):
+    """Two calls in a row.  Against paged_attn_fwd given a caller workspace of the same
+    32 MiB the plan is the same, so the results are bit for bit the same; against the
+    recommended workspace they agree within the parity tolerance, and the first call is
+    also held to the oracle."""
     a = to_device(wl.workload_attention(name))
-    ref_o, ref_l = run_gpu_attention(vas_lib, a)
+    same_o, same_l = run_gpu_attention(vas_lib, a, workspace_bytes=STATIC_BYTES)
+    rec_o, rec_l = run_gpu_attention(vas_lib, a)
     tol = TOL[a.kv_dtype]
-    for _ in range(2):  # the shared array keeps the previous call's contents
+    for call in range(2):  # the shared array keeps the previous call's contents
         out = torch.full_like(a.q, float("nan"))
         lse = torch.full((a.q.shape[0], a.q.shape[1]), float("nan"), device="cuda")
         assert _call_static(vas_lib, a, out, lse) == vas_lib.VAS_OK
         torch.cuda.synchronize()
-        o, r = out.double(), ref_o.double()
-        assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+        assert torch.equal(out, same_o) and torch.equal(lse, same_l)
+        o, r = out.double(), rec_o.double()
         assert (o - r).abs().max().item() <= tol["max_abs"]
         assert ((o - r).norm() / r.norm()).item() <= tol["rel_l2"]
-        assert (lse - ref_l).abs().max().item() <= tol["lse"]
+        assert (lse - rec_l).abs().max().item() <= tol["lse"]
+        if call == 0:
+            ref_o, ref_l = oracle_attention(a)
+            compare_attention(out, lse, ref_o, ref_l, a.kv_dtype)
     assert vas_lib.vas_last_device_error() == 0
 
 

@@ -1,5 +1,6 @@
 // Library-wide C ABI entry points: the device error word, status strings and the
 // diagnostic Philox kernel.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -15,9 +16,9 @@ namespace vas {
 __device__ int32_t g_error_word;
 
 namespace {
-constexpr int kMaxDevices = 64;
-int32_t* g_error_ptr[kMaxDevices];
+constexpr int kMaxDevices = kMaxCachedDevices;
 int g_sms[kMaxDevices];
+SymbolCache g_error_cache;
 std::mutex g_mu;
 
 int current_device() {
@@ -25,18 +26,51 @@ int current_device() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
   return dev;
 }
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Driver entry points, found through the runtime (the library does not link libcuda).
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
 }  // namespace
 
-int32_t* device_error_word() {
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+void* cached_symbol_address(SymbolCache& cache, const void* symbol) {
   const int dev = current_device();
   if (dev < 0) return nullptr;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_error_ptr[dev]) {
+  if (id == 0 || cache.ctx[dev] != id || !cache.ptr[dev]) {
+    // No context yet (the lookup below makes the device's primary context current), or
+    // a different one from the cached lookup's: resolve the address again.
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    g_error_ptr[dev] = static_cast<int32_t*>(p);
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+    cache.ptr[dev] = p;
+    cache.ctx[dev] = current_context_id();
   }
-  return g_error_ptr[dev];
+  return cache.ptr[dev];
+}
+
+int32_t* device_error_word() {
+  return static_cast<int32_t*>(cached_symbol_address(g_error_cache, &g_error_word));
 }
 
 int num_sms() {

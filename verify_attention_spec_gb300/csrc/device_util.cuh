@@ -184,6 +184,87 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Bulk copy global -> shared without an L2 hint; same rules as bulk_load.
+__device__ __forceinline__ void bulk_load_plain(void* dst, const void* src, uint32_t bytes,
+                                                uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- float-float arithmetic ---------------------------------------------------------
+// A sum carried as an unevaluated pair hi + lo of fp32 numbers (|lo| <= half an ulp of
+// hi), built from error-free transformations: Knuth's TwoSum, Dekker's Fast2Sum and the
+// fused-multiply-add form of TwoProduct.  About 44 significant bits at fp32 instruction
+// cost; on this part a double-precision instruction costs an order of magnitude more.
+struct ff32 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff32 ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// Renormalise s + e with |e| small against |s| (Fast2Sum).
+__device__ __forceinline__ ff32 ff_fast_two_sum(float s, float e) {
+  const float hi = __fadd_rn(s, e);
+  return {hi, __fsub_rn(e, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ ff32 ff_add(ff32 a, ff32 b) {
+  const ff32 s = ff_two_sum(a.hi, b.hi);
+  return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ ff32 ff_add_f(ff32 a, float b) {
+  const ff32 s = ff_two_sum(a.hi, b);
+  return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+__device__ __forceinline__ ff32 ff_mul(ff32 a, ff32 b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  const float e = __fmaf_rn(a.hi, b.hi, -p);
+  return ff_fast_two_sum(p, __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, e)));
+}
+
+// a > b for normalised pairs.
+__device__ __forceinline__ bool ff_gt(ff32 a, ff32 b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ ff32 ff_from_double(double d) {
+  const float hi = __double2float_rn(d);
+  return {hi, __double2float_rn(d - (double)hi)};
+}
+
+__device__ __forceinline__ double ff_to_double(ff32 a) { return (double)a.hi + (double)a.lo; }
+
+__device__ __forceinline__ ff32 ff_shfl_xor(ff32 a, int o) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+
+__device__ __forceinline__ ff32 ff_shfl_up(ff32 a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+
+__device__ __forceinline__ ff32 ff_shfl(ff32 a, int src) {
+  return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
+// Split cluster barrier: every thread of every CTA in the cluster arrives once and waits
+// once, alternately.  Arrive has release semantics, wait acquire semantics.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // The two halves of a bf16 pair as fp32 (exact: a bf16 is the top half of an fp32).
 __device__ __forceinline__ float bf16_lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

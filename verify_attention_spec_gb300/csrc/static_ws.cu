@@ -10,9 +10,9 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "../../include/vas.h"
+#include "vas_internal.h"
 
 namespace vas {
 namespace {
@@ -24,23 +24,15 @@ constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;
 
 static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_static_ptr[kMaxDevices];
-std::mutex g_static_mu;
+SymbolCache g_static_cache;
 
 // Device address of this device's copy of the array.  In host code the array's name is
-// only a stand-in for the symbol, so the address comes from the runtime, once per device
-// and with that device current.
+// only a stand-in for the symbol, so the address comes from the runtime: looked up with
+// that device current on the first call, and again whenever the device's context has
+// changed since (a context destroyed by cudaDeviceReset and created anew holds the
+// array at a new address).
 void* static_workspace_address() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
-    g_static_ptr[dev] = p;
-  }
-  return g_static_ptr[dev];
+  return cached_symbol_address(g_static_cache, &g_static_workspace);
 }
 
 }  // namespace

@@ -40,7 +40,7 @@ spec_verify, their K/V stored as FP8 E4M3 or INT8 codes with one fp32 scale per
 scale = max |x| over the head's D values / 448 (E4M3) or / 127 (INT8), code = x / scale
 rounded to nearest (E4M3 by torch's float8_e4m3fn conversion).
 
-Distributions (the pages leave them open; readings stated in the design doc): N(0, s) means
+Distributions (the pages leave them open; the plainest readings are taken): N(0, s) means
 standard deviation s; log-normal L = round(exp(ln median + sigma z)); Pareto
 L = floor(x_min (1 - U)^(-1/alpha)); uniform integers inclusive; p = softmax(logits),
 logits ~ N(0, s_p); q = softmax(logits + N(0, s_q) noise); drafts x_i ~ q_i.  The page
