@@ -329,6 +329,14 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool
 namespace vas {
 
 // L2 policy for data re-read by later work of the same call.
+// L2 policy for data that other CTAs read again soon (a prompt chunk's pages, read by
+// each of its row blocks).
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));

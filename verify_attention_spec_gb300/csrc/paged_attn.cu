@@ -1117,7 +1117,10 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------ producer ------------------------------
-    const uint64_t pol = l2_policy_evict_first();
+    // KV of decode and verify units is read once per call; a prompt chunk's pages are
+    // read by each of its row blocks, so they are kept in L2 as long as other data.
+    const uint64_t pol_once = l2_policy_evict_first();
+    const uint64_t pol_shared = l2_policy_evict_normal();
     uint32_t stage_it = 0, unit_it = 0;
     bool ok = true;
     // Descriptor pipeline: unit u is streamed while the next unit's descriptor and
@@ -1178,6 +1181,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
       if (it.seq >= 0) {
         const int head = u % a.Hkv;
         const int32_t* bt_row = a.block_table + (size_t)it.seq * a.maxp;
+        const uint64_t pol = a.G * sp.qlen > kRowBlock ? pol_shared : pol_once;
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
           const int npg = min(32, it.page_end - pg0);
           const int32_t my_id =
@@ -2502,6 +2506,13 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
   pa.items_cap = lay.items_cap;
   pa.partial_cap = lay.partial_cap;
   pa.err = err;
+  // Tensor maps first, so that the plan and the attention grid are launched back to back.
+  CUtensorMap mk, mv;
+  if (quant && (!encode_code_map(&mk, k_pages, dims) || !encode_code_map(&mv, v_pages, dims)))
+    return VAS_E_CUDA;
+  if (!quant && bf16 &&
+      (!encode_pool_map(&mk, k_pages, dims) || !encode_pool_map(&mv, v_pages, dims)))
+    return VAS_E_CUDA;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
@@ -2548,9 +2559,6 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
   aa.v_scale = v_scale;
 
   if (quant) {
-    CUtensorMap mk, mv;
-    if (!encode_code_map(&mk, k_pages, dims) || !encode_code_map(&mv, v_pages, dims))
-      return VAS_E_CUDA;
     const int grid = sms;
     const bool fp8 = d.kv_dtype == VAS_FP8_E4M3;
     if (d.head_dim == 128 && d.page_size == 16)
@@ -2566,9 +2574,6 @@ int attn_launch(const void* q, const void* k_pages, const void* v_pages, const f
                : launch_bf16<64, 32, kKvInt8>(mk, mv, aa, grid, stream);
   }
   if (bf16) {
-    CUtensorMap mk, mv;
-    if (!encode_pool_map(&mk, k_pages, dims) || !encode_pool_map(&mv, v_pages, dims))
-      return VAS_E_CUDA;
     const int grid = sms;
     if (d.head_dim == 128 && d.page_size == 16)
       return launch_bf16<128, 16, kKvBf16>(mk, mv, aa, grid, stream);
