@@ -145,3 +145,56 @@ def test_zero_residual_fallback_matches_oracle(vas_lib):
     compare_verify(acc, out, ref)
     if np.any(ref.fallback):
         assert vas_lib.vas_last_device_error() & vas_lib.VAS_DEV_RESIDUAL_FALLBACK
+
+
+@pytest.mark.parametrize("V", [1_048_576, 999_999])
+def test_largest_vocabularies(vas_lib, V):
+    """The largest vocabulary the kernel takes (8 slices of 64 stages of 2048 tokens), and
+    one just below it that is not a multiple of 4 (rows not 16-byte aligned: staged by
+    plain loads)."""
+    v = wl.verify_inputs(3, 2, V, seed=V % 1000, p_logit_std=3.0, q_noise_std=1.5)
+    for seed in (5, 6):
+        ref = oracle.spec_verify(v.p, v.q, v.draft, seed)
+        acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, seed)
+        compare_verify(acc, out, ref)
+    assert vas_lib.vas_last_device_error() == 0
+
+
+def test_vocabulary_beyond_the_limit_is_rejected(vas_lib):
+    """One token past the largest vocabulary: VAS_E_UNSUPPORTED from the host, nothing
+    launched (the outputs keep their contents)."""
+    V = 1_048_577
+    B, k = 1, 1
+    p = torch.full((B, k + 1, V), 1.0 / V, device="cuda")
+    q = torch.full((B, k, V), 1.0 / V, device="cuda")
+    x = torch.zeros((B, k), dtype=torch.int32, device="cuda")
+    acc = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((B, k + 1), -7, dtype=torch.int32, device="cuda")
+    st = vas_lib._lib.spec_verify(p.data_ptr(), q.data_ptr(), x.data_ptr(), 1, acc.data_ptr(),
+                                  out.data_ptr(), B, k, V, None)
+    assert st == vas_lib.VAS_E_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(acc == -7) and torch.all(out == -7)
+
+
+def test_misaligned_rows_take_the_plain_path(vas_lib):
+    """p and q starting 4 bytes past a 16-byte boundary (a vocabulary that is a multiple
+    of 4 but rows that are not 16-byte aligned) give the same tokens as aligned copies."""
+    v = wl.verify_inputs(40, 3, 4096, seed=21, p_logit_std=2.0, q_noise_std=1.0)
+    ref = oracle.spec_verify(v.p, v.q, v.draft, 8)
+    pbuf = torch.empty(v.p.size + 1, dtype=torch.float32, device="cuda")
+    qbuf = torch.empty(v.q.size + 1, dtype=torch.float32, device="cuda")
+    pd = pbuf[1:].view(v.p.shape)
+    qd = qbuf[1:].view(v.q.shape)
+    pd.copy_(torch.from_numpy(v.p))
+    qd.copy_(torch.from_numpy(v.q))
+    assert pd.data_ptr() % 16 == 4
+    xd = torch.from_numpy(v.draft).cuda()
+    acc = torch.empty(v.B, dtype=torch.int32, device="cuda")
+    out = torch.empty(v.B, v.k + 1, dtype=torch.int32, device="cuda")
+    vas_lib.spec_verify(pd, qd, xd, 8, acc, out)
+    torch.cuda.synchronize()
+    compare_verify(acc.cpu().numpy(), out.cpu().numpy(), ref)
+    aligned = run_gpu_verify(vas_lib, v.p, v.q, v.draft, 8)
+    np.testing.assert_array_equal(acc.cpu().numpy(), aligned[0])
+    np.testing.assert_array_equal(out.cpu().numpy(), aligned[1])
