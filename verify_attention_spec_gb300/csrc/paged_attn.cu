@@ -1943,11 +1943,14 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
         break;
       }
       const float* buf = reinterpret_cast<const float*>(scratch);
-      const int d = warp * 32 + lane;  // this lane's output column
+      // Per row: the weight of each warp's partition and 1 / l, one thread per row; then
+      // every lane writes its column of each row.
       // Warp w took the stages with (stage0 + si) % 4 == w.  Summing the partitions in
       // the order of si % 4, not of w, makes the result independent of stage0, i.e. of
       // which units this CTA happened to run before: reruns are bit-identical.
-      for (int r = 0; r < Rb; ++r) {
+      float* coef = reinterpret_cast<float*>(scratch + S::kNarrowBytes);  // [row][8]
+      if (tid < Rb) {
+        const int r = tid;
         float mw[kConsumerWarps], M = -INFINITY;
 #pragma unroll
         for (int pt = 0; pt < kConsumerWarps; ++pt) {
@@ -1956,26 +1959,38 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
           M = fmaxf(M, mw[pt]);
         }
         const float mu = M == -INFINITY ? 0.f : M;
-        float Lsum = 0.f, acc = 0.f;
+        float Lsum = 0.f;
 #pragma unroll
         for (int pt = 0; pt < kConsumerWarps; ++pt) {
           const int w = (stage0 + pt) % kConsumerWarps;
           const float f = exp2f(mw[pt] - mu);
           Lsum += f * buf[w * S::kNarrowWarpFloats + kNarrowRows * S::kNarrowStride + kNarrowRows + r];
-          if (d < D) acc += f * buf[w * S::kNarrowWarpFloats + r * S::kNarrowStride + d];
+          coef[r * 8 + pt] = f;
         }
-        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        coef[r * 8 + 4] = Lsum > 0.f ? 1.f / Lsum : 0.f;
         float row_lse = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-        float x = acc * inv;
-        if (poison) row_lse = x = NAN;
-        if (sp.nsplit == 1) {
-          const size_t orow = out_row(a, sp, head, r0 + r);
-          if (d < D) static_cast<__nv_bfloat16*>(a.out)[orow * D + d] = __float2bfloat16(x);
-          if (warp == 0 && lane == 0) a.lse[orow] = row_lse;
-        } else {
-          const size_t prow = partial_row(a, sp, split, head, r0 + r);
-          if (d < D) a.part_o[prow * D + d] = x;
-          if (warp == 0 && lane == 0) a.part_lse[prow] = row_lse;
+        if (poison) row_lse = NAN;
+        if (sp.nsplit == 1) a.lse[out_row(a, sp, head, r0 + r)] = row_lse;
+        else a.part_lse[partial_row(a, sp, split, head, r0 + r)] = row_lse;
+      }
+      named_bar_sync(1, kConsumerThreads);
+      const int d = warp * 32 + lane;  // this lane's output column
+      if (d < D) {
+#pragma unroll 1
+        for (int r = 0; r < Rb; ++r) {
+          const float4 f = *reinterpret_cast<const float4*>(coef + r * 8);
+          const float fw[kConsumerWarps] = {f.x, f.y, f.z, f.w};
+          float acc = 0.f;
+#pragma unroll
+          for (int pt = 0; pt < kConsumerWarps; ++pt) {
+            const int w = (stage0 + pt) % kConsumerWarps;
+            acc = fmaf(fw[pt], buf[w * S::kNarrowWarpFloats + r * S::kNarrowStride + d], acc);
+          }
+          const float x = poison ? NAN : acc * coef[r * 8 + 4];
+          if (sp.nsplit == 1)
+            static_cast<__nv_bfloat16*>(a.out)[out_row(a, sp, head, r0 + r) * D + d] = __float2bfloat16(x);
+          else
+            a.part_o[partial_row(a, sp, split, head, r0 + r) * D + d] = x;
         }
       }
     } else {
