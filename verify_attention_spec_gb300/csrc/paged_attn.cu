@@ -1008,8 +1008,21 @@ __device__ void merge_splits(const AttnArgs& a, const SeqPlan& sp, int head, int
 struct PendingMerge {
   SeqPlan sp;
   int32_t head, r0, Rb, valid;
-  int32_t old;  // thread 0 only: the counter's value before this CTA's arrival
+  int32_t old;   // thread 0 only: the counter's value before this CTA's arrival
+  int32_t* ctr;  // thread 0 only: the counter
 };
+
+// Acquire and release at GPU scope on one 32-bit word.
+__device__ __forceinline__ int32_t load_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int32_t atomic_add_release_gpu(int32_t* p, int32_t x) {
+  int32_t old;
+  asm volatile("atom.release.gpu.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(x) : "memory");
+  return old;
+}
 
 // All consumer threads: the CTA's partial rows have been written.
 __device__ __forceinline__ void count_split_arrival(const AttnArgs& a, const SeqPlan& sp,
@@ -1018,8 +1031,9 @@ __device__ __forceinline__ void count_split_arrival(const AttnArgs& a, const Seq
   named_bar_sync(1, kConsumerThreads);  // every partial store of the CTA is issued
   if (threadIdx.x == 0) {
     const int rb = it.split_rb & ((1 << kRbBits) - 1);
+    pm.ctr = a.counters + ((size_t)sp.item0 + rb) * a.Hkv + head;
     __threadfence();  // orders the CTA's partials before the count (cumulative via the barrier)
-    pm.old = atomicAdd(a.counters + ((size_t)sp.item0 + rb) * a.Hkv + head, 1);
+    pm.old = atomicAdd(pm.ctr, 1);
   }
   pm.sp = sp;
   pm.head = head;
@@ -1028,14 +1042,22 @@ __device__ __forceinline__ void count_split_arrival(const AttnArgs& a, const Seq
   pm.valid = 1;
 }
 
-// All consumer threads; `flag` was set by thread 0 before the last named barrier.
+// Thread 0, before the named barrier that precedes finish_pending: whether this CTA
+// counted the last split of its previous unit.  If so, an acquire read of the counter
+// (which holds every split's released count) orders the other CTAs' partials before
+// the barrier, and so before every consumer's reads of them.
+__device__ __forceinline__ int32_t last_split_seen(const PendingMerge& pm) {
+  const bool last = pm.valid && pm.old == pm.sp.nsplit - 1;
+  if (last) (void)load_acquire_gpu(pm.ctr);
+  return last;
+}
+
+// All consumer threads; `flag` was set by thread 0 (last_split_seen) before the last
+// named barrier.
 template <int D>
 __device__ __forceinline__ void finish_pending(const AttnArgs& a, PendingMerge& pm,
                                                const int32_t* flag, int warp, int lane) {
-  if (pm.valid && *flag) {
-    __threadfence();
-    merge_splits<D>(a, pm.sp, pm.head, pm.r0, pm.Rb, warp, lane);
-  }
+  if (pm.valid && *flag) merge_splits<D>(a, pm.sp, pm.head, pm.r0, pm.Rb, warp, lane);
   pm.valid = 0;
 }
 
@@ -1573,7 +1595,7 @@ __global__ void __launch_bounds__(KQ == kKvBf16 ? kThreads : kThreadsQ, 1)
   for (;;) {
     const int slot = unit_it % kRing;
     const bool got = mbar_wait(&ufull[slot], (unit_it / kRing) & 1);
-    if (tid == 0) *flag = pm.valid && pm.old == pm.sp.nsplit - 1;
+    if (tid == 0) *flag = last_split_seen(pm);
     RingEntry re;
     re.u = -1;
     if (got) re = ring[slot];
