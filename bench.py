@@ -637,8 +637,9 @@ def run_ours(args):
 
     # e2e: the same step through the C ABI from pinned host buffers, as a serving loop
     # runs it: every step's inputs are copied from pinned host memory and its results
-    # read back, on a copy stream, double-buffered so that the copies of steps i + 1 and
-    # i - 1 overlap the compute of step i (the KV page pool is the cache: it stays).
+    # read back, on one copy stream per direction, double-buffered so that the copies of
+    # steps i + 1 and i - 1 overlap the compute of step i (the KV page pool is the cache:
+    # it stays).
     e2e = None
     if not args.no_e2e:
         host_in = [t.cpu().pin_memory() for t in (a.q, a.block_table, a.seq_lens, a.query_lens)]
@@ -646,7 +647,8 @@ def run_ours(args):
                   if v is not None else [])
         res_like = [out, lse] + ([acc_d, tok_d] if v is not None else [])
         cs = torch.cuda.current_stream()
-        xs = torch.cuda.Stream()
+        xs = torch.cuda.Stream()  # host-to-device copies
+        ds = torch.cuda.Stream()  # device-to-host copies: the other direction's engine
         slots = []
         for _ in range(2):
             slots.append(dict(
@@ -675,11 +677,11 @@ def run_ours(args):
             sl["comp"].record(cs)
 
         def download(sl):
-            with torch.cuda.stream(xs):
-                xs.wait_event(sl["comp"])
+            with torch.cuda.stream(ds):
+                ds.wait_event(sl["comp"])
                 for dd, hdst in zip(sl["dout"], sl["hout"]):
                     hdst.copy_(dd, non_blocking=True)
-                sl["down"].record(xs)
+                sl["down"].record(ds)
 
         def e2e_run(n, t0=None, t1=None):
             if t0 is not None:
@@ -691,6 +693,7 @@ def run_ours(args):
                 compute(slots[i % 2])
                 download(slots[i % 2])
             if t1 is not None:
+                xs.wait_stream(ds)  # the last results are read back
                 t1.record(xs)
 
         e2e_run(max(args.warmup, 2))
