@@ -21,7 +21,7 @@
 // totals meet through distributed shared memory after one cluster barrier, so every CTA
 // agrees on S and on the slice holding the target s_j * S.  That CTA walks its stage and
 // tile totals to the tile holding the target, reads only that tile again (from L2), scans
-// its lanes in fp64, and the crossing lane walks its 8 elements.  Rows that are not
+// its lanes as float-float pairs, and the crossing lane walks its 8 elements.  Rows that are not
 // 16-byte aligned (a vocabulary that is not a multiple of 4) are staged by plain loads.
 // Uniforms come from Philox4x32-10 keyed by the seed with counter (position, sequence,
 // 0, 0).
