@@ -48,3 +48,52 @@ def test_unique_kv_bytes_counts_shared_pages_once():
     # without sharing it equals the per-sequence count
     bt2 = np.array([[5, 6, 1], [7, 8, 2]])
     assert bench.unique_kv_bytes(bt2, [40, 35], 2, 8, 16, 2) == (40 + 35) * 2 * 8 * 2 * 2
+
+
+def test_acceptance_stats_counts_tests_run_and_sum_of_minima():
+    # Sequences accepting 0, 4 and 2 of k = 4 drafts ran 1, 4 and 3 ratio tests.
+    acc = np.array([0, 4, 2])
+    p = np.zeros((3, 5, 4))
+    q = np.zeros((3, 4, 4))
+    p[:, :, :2] = 0.5                 # p = (1/2, 1/2, 0, 0) at every position
+    q[:] = 0.25                       # q uniform: sum_x min(p, q) = 1/2
+    q[2, 3] = [0.5, 0.5, 0.0, 0.0]    # one position with q = p: sum of minima 1
+    st = bench.acceptance_stats(acc, 4, p, q)
+    assert st["mean_accepted"] == 2.0
+    assert st["per_token_acceptance"] == 6 / 8
+    assert np.isclose(st["alpha_sum_min_pq"], (0.5 + 0.5 + (0.5 * 3 + 1.0) / 4) / 3)
+    assert "alpha_sum_min_pq" not in bench.acceptance_stats(acc, 4)
+
+
+def test_verify_bytes_reads_two_rows_after_a_rejection_and_one_after_full_acceptance():
+    k, V = 4, 10
+    scalars = k * 4 + k * 8 + (k + 1) * 4 + 4  # drafts, p and q at them, outputs, length
+    assert bench.verify_bytes([0, 4], k, V) == (2 + 1) * V * 4 + 2 * scalars
+    assert bench.verify_bytes([4, 4, 4], k, V) == 3 * V * 4 + 3 * scalars
+
+
+def test_tree_verify_bytes_by_where_the_walk_ends():
+    # Node 0 is the root; drafts 1..3 with parents 0, 1, 0 (draft i is node i).
+    parents = np.array([[0, 1, 0], [0, 1, 0]])
+    path = np.array([[1, 2, 0], [1, 0, 0]])
+    V, n = 16, 3
+    per_seq = n * 4 * 3 + n * 8 + (n + 1) * 4 + 4
+    # Sequence 0 accepted the chain 1 -> 2 (node 2 is a leaf: its p row alone); sequence 1
+    # accepted node 1, which has a child (p and q rows).
+    assert bench.tree_verify_bytes([2, 1], path, parents, V) == (1 + 2) * V * 4 + 2 * per_seq
+
+
+def test_ncu_traffic_is_dropped_when_the_kernel_source_changed(tmp_path, monkeypatch):
+    csrc = tmp_path / "verify_attention_spec_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES["paged_attn"]:
+        (csrc / f).write_text("// kernel " + f + "\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash("paged_attn")
+    prof = tmp_path / "profiles" / "paged_attn_w_ncu.md"
+    prof.write_text(f"kernel_source_sha256_16: {h}\ndram_bytes_per_full_launch: 12345\n")
+    assert bench.ncu_traffic("w") == 12345.0
+    assert bench.ncu_traffic("other") is None
+    (csrc / bench.KERNEL_SOURCES["paged_attn"][0]).write_text("// changed\n")
+    assert bench.ncu_traffic("w") is None
