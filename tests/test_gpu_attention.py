@@ -77,6 +77,24 @@ def test_split_invariance(vas_lib):
     assert (l1 - l2).abs().max().item() <= 1e-4
 
 
+def test_many_splits(vas_lib):
+    """Contexts of 70000 tokens split into more pieces than a warp has lanes: a decode
+    sequence (narrow units) and a k=4 verify sequence (wide units), 35 and 38 splits on a
+    152-SM part, each merged by the CTA that finishes its last split.  Against the
+    oracle, and against the unsplit result."""
+    a = _case([70000, 70000, 40], [1, 5, 1], Hq=32, Hkv=8, D=128, P=16, seed=31)
+    ref_o, ref_l = oracle_attention(a)
+    ad = to_device(a)
+    out, lse = run_gpu_attention(vas_lib, ad)
+    compare_attention(out, lse, ref_o, ref_l, wl.BF16)
+    dims = vas_lib.attn_dims(ad.q, ad.k_pages, ad.block_table, ad.seq_lens)
+    o1, l1 = run_gpu_attention(vas_lib, ad, workspace_bytes=vas_lib.paged_attn_workspace_min(dims))
+    compare_attention(o1, l1, ref_o, ref_l, wl.BF16)
+    assert (o1.float() - out.float()).abs().max().item() <= 2 ** -7
+    assert (l1 - lse).abs().max().item() <= 1e-4
+    assert vas_lib.vas_last_device_error() == 0
+
+
 @pytest.mark.parametrize("name", ["decode64", "verify32", "mixed272"])
 def test_deterministic_reruns(vas_lib, name):
     """Same inputs, same bits, whichever SM and CTA ends up with which work unit."""
