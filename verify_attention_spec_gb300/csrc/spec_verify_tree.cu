@@ -18,7 +18,8 @@
 // Philox(c - 1, b), the draw at node u uses word 1 of Philox(u, b).
 //
 // Kernel: one thread-block cluster of C CTAs per sequence (C <= 8, fewer for small
-// vocabularies); CTA r owns slice r of the vocabulary.  Every CTA takes the same
+// vocabularies and for batches that would not fit four CTAs per SM); CTA r owns slice r
+// of the vocabulary.  Every CTA takes the same
 // decisions (thread 0, from the same values), so the clusters' CTAs walk in step.  A
 // pass covers each slice in tiles of 256 consecutive elements, 8 contiguous per lane:
 // each lane sums its 8 weights, the warp scans the 32 lane sums (fp32, lane order) and
@@ -72,6 +73,12 @@ constexpr int kTile = 32 * kLaneElems;
 constexpr int kMaxCluster = 8;
 constexpr int kSliceMin = 4096;     // smallest vocabulary slice per CTA
 constexpr int kMaxTiles = 160;      // tiles per slice: vocabularies up to 8 x 160 x 256
+// One tile per warp in flight keeps the kernel at 64 registers, so four CTAs share an SM
+// and a batch of 64 trees still gets eight CTAs per tree: shorter passes, which is what
+// the walk's chain of passes waits on (four tiles in flight at two CTAs per SM measured
+// 94 us on 64 trees over V = 128256, this 80 us).
+constexpr int kTilesPerIter = 1;
+constexpr int kCtasPerSm = 4;
 constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTiles * kTile;
 
 // One lane's 8 inputs from x0 (past V: zero), as two float4 loads per row when the
@@ -134,18 +141,17 @@ __device__ double pass_totals(const float* pu, const float* qu, int xb, int V, f
   if (threadIdx.x == 0) *s_last = -1;
   __syncthreads();
   int last = -1;
-  // Four tiles per iteration keep several loads of each lane in flight.
-  for (int t0 = warp * 4; t0 < n_tiles; t0 += kWarps * 4) {
-    // All four tiles' loads go out before any of them is used.
-    float p8[4][kLaneElems], q8[4][kLaneElems];
+  // kTilesPerIter tiles per iteration: their loads all go out before any is used.
+  for (int t0 = warp * kTilesPerIter; t0 < n_tiles; t0 += kWarps * kTilesPerIter) {
+    float p8[kTilesPerIter][kLaneElems], q8[kTilesPerIter][kLaneElems];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kTilesPerIter; ++j) {
       const int x0 = xb + (t0 + j) * kTile + lane * kLaneElems;
       if (t0 + j < n_tiles) lane_load(pu, qu, x0, V, vec, p8[j], q8[j]);
     }
-    float v[4];
+    float v[kTilesPerIter];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kTilesPerIter; ++j) {
       const int x0 = xb + (t0 + j) * kTile + lane * kLaneElems;
       v[j] = 0.f;
       if (t0 + j < n_tiles)
@@ -157,7 +163,7 @@ __device__ double pass_totals(const float* pu, const float* qu, int xb, int V, f
         }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kTilesPerIter; ++j) {
       const float tile = warp_inclusive_scan(v[j]);
       if (lane == 31 && t0 + j < n_tiles) s_tile[t0 + j] = tile;
     }
@@ -175,7 +181,7 @@ __device__ double pass_totals(const float* pu, const float* qu, int xb, int V, f
   return *s_total;
 }
 
-__global__ void __launch_bounds__(kThreads, 2) spec_verify_tree_kernel(const Args a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(const Args a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -391,11 +397,11 @@ extern "C" int spec_verify_tree(const float* p, const float* q, const int32_t* d
   // Cluster size and slices as for spec_verify: slices of at least kSliceMin elements,
   // whole tiles.
   // Each sequence's walk is long-lived: with many sequences, fewer CTAs per sequence
-  // keep the whole grid resident (two CTAs per SM).
+  // keep the whole grid resident (kCtasPerSm CTAs per SM).
   int C = (V + kSliceMin - 1) / kSliceMin;
   if (C > kMaxCluster) C = kMaxCluster;
   const int sms = vas::num_sms();
-  while (C > 1 && (int64_t)B * C > 2LL * (sms > 0 ? sms : 148)) --C;
+  while (C > 1 && (int64_t)B * C > (int64_t)kCtasPerSm * (sms > 0 ? sms : 148)) --C;
   int slice = (V + C - 1) / C;
   slice = (slice + kTile - 1) / kTile * kTile;
   C = (V + slice - 1) / slice;
