@@ -98,6 +98,7 @@ constexpr int kPreciseTokens = 64;
 constexpr int32_t kItemPrecise = 1 << 30;
 constexpr int kPlanThreads = 256;
 constexpr int kOrderBuckets = 64;  // page-count classes of the work order
+constexpr int kWideOrderWeight = 2;  // a wide unit's page counts twice in the work order
 constexpr int kPlanSmemSeqs = 4096;
 constexpr int kSeqInvalid = 1;
 
@@ -393,9 +394,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
 #pragma unroll
     for (int k = 0; k < 3; ++k) carry[k] += t[k];
   }
-  // Work order: the items by decreasing page count (kOrderBuckets buckets up to the
-  // split length), so that the longest units start first and the grid ends on short
-  // ones (a unit's place in the order changes only which CTA runs it and when).
+  // Work order: the items by decreasing estimated time (kOrderBuckets buckets up to the
+  // longest), so that the longest units start first and the grid ends on short ones (a
+  // unit's place in the order changes only which CTA runs it and when).  The estimate is
+  // the page count, doubled for wide units (17..64 rows per KV head), which stream at
+  // about half the rate of narrow ones.
   {
     __shared__ int32_t hist[kOrderBuckets];
     const int64_t n_items = carry[1] < a.items_cap ? carry[1] : a.items_cap;
@@ -403,7 +406,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanArgs a) {
     const int64_t span = cmax < (int64_t)a.maxp ? cmax : (int64_t)a.maxp;  // longest item
     auto bucket = [&](int64_t i) {
       const Item& t = a.items[i];
-      const int64_t b = (int64_t)(t.page_end - t.page_begin) * kOrderBuckets / (span + 1);
+      int w = 1;
+      if (t.seq >= 0) {
+        const int R = a.G * (cached ? s_ql[t.seq] : a.query_lens[t.seq]);
+        if (R > kNarrowRows && R <= kRowBlock) w = kWideOrderWeight;
+      }
+      const int64_t b = (int64_t)(t.page_end - t.page_begin) * w * kOrderBuckets /
+                        (kWideOrderWeight * span + 1);
       return (int)(b < 0 ? 0 : (b < kOrderBuckets ? b : kOrderBuckets - 1));
     };
     for (int b = tid; b < kOrderBuckets; b += kPlanThreads) hist[b] = 0;
