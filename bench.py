@@ -217,7 +217,8 @@ class ClockSampler:
 # valid only while the kernel source is unchanged.
 # ---------------------------------------------------------------------------------
 KERNEL_SOURCES = {"paged_attn": ["paged_attn.cu", "device_util.cuh"],
-                  "spec_verify": ["spec_verify.cu", "device_util.cuh", "philox.cuh"]}
+                  "spec_verify": ["spec_verify.cu", "device_util.cuh", "philox.cuh"],
+                  "spec_verify_tree": ["spec_verify_tree.cu", "device_util.cuh", "philox.cuh"]}
 
 
 def kernel_source_hash(kernel="paged_attn"):
@@ -773,7 +774,8 @@ def run_ours(args):
                               "gbs": ver_gbs, "algorithmic_bytes": v_bytes,
                               "frac_of_measured_peak": ver_gbs / peak,
                               "frac_of_nominal_8tbs": ver_gbs / NOMINAL_HBM_GBS,
-                              "traffic": ncu_traffic(name, "spec_verify"),
+                              "traffic": ncu_traffic(name, "spec_verify" if v.parents is None
+                                                     else "spec_verify_tree"),
                               **(acceptance_stats(acc, v.k, v.p, v.q) if v.parents is None
                                  else acceptance_stats(acc, v.k))}
     if e2e is not None:
