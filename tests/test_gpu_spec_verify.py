@@ -198,3 +198,19 @@ def test_misaligned_rows_take_the_plain_path(vas_lib):
     aligned = run_gpu_verify(vas_lib, v.p, v.q, v.draft, 8)
     np.testing.assert_array_equal(acc.cpu().numpy(), aligned[0])
     np.testing.assert_array_equal(out.cpu().numpy(), aligned[1])
+
+
+def test_longest_draft_window(vas_lib):
+    """k = 255, the largest window: random rows, and rows with q = p, where every draft is
+    accepted and the token after them comes from the bonus row p_k."""
+    v = wl.verify_inputs(3, 255, 64, seed=255, p_logit_std=2.0, q_noise_std=1.0)
+    for seed in (3, 4):
+        ref = oracle.spec_verify(v.p, v.q, v.draft, seed)
+        acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, seed)
+        compare_verify(acc, out, ref)
+    same_q = np.ascontiguousarray(v.p[:, :255])
+    ref = oracle.spec_verify(v.p, same_q, v.draft, 9)
+    acc, out = run_gpu_verify(vas_lib, v.p, same_q, v.draft, 9)
+    compare_verify(acc, out, ref)
+    assert np.all(acc == 255)
+    assert vas_lib.vas_last_device_error() == 0

@@ -61,9 +61,10 @@ def _compare(acc, out, path, ref):
 
 
 # (200, 4, 50003): more trees than fit eight CTAs each, so the clusters shrink to three
-# CTAs, with a vocabulary whose rows are not 16-byte aligned.
+# CTAs, with a vocabulary whose rows are not 16-byte aligned; (8, 255, 64): the largest
+# tree.
 @pytest.mark.parametrize("B,n,V", [(64, 8, 5), (64, 16, 1000), (32, 63, 257), (64, 6, 128256),
-                                   (200, 4, 50003)])
+                                   (200, 4, 50003), (8, 255, 64)])
 def test_random_trees_match_the_oracle(vas_lib, B, n, V):
     rng = np.random.default_rng(B + n + V)
     p, q, x, parents = _tree_inputs(rng, B, n, V)
