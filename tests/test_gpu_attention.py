@@ -95,6 +95,19 @@ def test_many_splits(vas_lib):
     assert vas_lib.vas_last_device_error() == 0
 
 
+def test_more_sequences_than_the_plan_caches(vas_lib):
+    """4500 sequences, more than the plan keeps in shared memory (4096): it reads the
+    lengths from global memory.  Decode and short verify windows, against the oracle."""
+    rng = np.random.default_rng(45)
+    lens = rng.integers(1, 90, size=4500)
+    qlens = np.where(rng.random(4500) < 0.1, np.minimum(lens, 3), 1)
+    a = _case(lens, qlens, Hq=4, Hkv=1, D=64, P=16, seed=45)
+    ref_o, ref_l = oracle_attention(a)
+    out, lse = run_gpu_attention(vas_lib, to_device(a))
+    compare_attention(out, lse, ref_o, ref_l, wl.BF16)
+    assert vas_lib.vas_last_device_error() == 0
+
+
 @pytest.mark.parametrize("name", ["decode64", "verify32", "mixed272"])
 def test_deterministic_reruns(vas_lib, name):
     """Same inputs, same bits, whichever SM and CTA ends up with which work unit."""
