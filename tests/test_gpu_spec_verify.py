@@ -214,3 +214,14 @@ def test_longest_draft_window(vas_lib):
     compare_verify(acc, out, ref)
     assert np.all(acc == 255)
     assert vas_lib.vas_last_device_error() == 0
+
+
+def test_more_clusters_than_fit_at_once(vas_lib):
+    """300 windows over V = 128256: 2400 CTAs, about four times what is resident at once,
+    so the clusters run in several waves."""
+    v = wl.verify_inputs(300, 2, 128256, seed=300)
+    ref = oracle.spec_verify(v.p, v.q, v.draft, 11)
+    acc, out = run_gpu_verify(vas_lib, v.p, v.q, v.draft, 11)
+    flagged, differ = compare_verify(acc, out, ref)
+    assert differ <= 1
+    assert vas_lib.vas_last_device_error() == 0
