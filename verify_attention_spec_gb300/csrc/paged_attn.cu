@@ -1021,16 +1021,11 @@ struct PendingMerge {
   int32_t* ctr;  // thread 0 only: the counter
 };
 
-// Acquire and release at GPU scope on one 32-bit word.
+// A 32-bit load with acquire semantics at GPU scope.
 __device__ __forceinline__ int32_t load_acquire_gpu(const int32_t* p) {
   int32_t v;
   asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-__device__ __forceinline__ int32_t atomic_add_release_gpu(int32_t* p, int32_t x) {
-  int32_t old;
-  asm volatile("atom.release.gpu.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(x) : "memory");
-  return old;
 }
 
 // All consumer threads: the CTA's partial rows have been written.
