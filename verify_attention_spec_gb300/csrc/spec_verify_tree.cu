@@ -24,8 +24,8 @@
 // pass covers each slice in tiles of 256 consecutive elements, 8 contiguous per lane:
 // each lane sums its 8 weights, the warp scans the 32 lane sums (fp32, lane order) and
 // the last lane's value is the tile's total, kept in shared memory; tile totals add up
-// in fp64 to the slice total, published to the cluster, and every CTA adds the C slice
-// totals in rank order.  A draw finds the slice, then the tile where the inverse CDF
+// in fp64 to the slice total, which each CTA stores into every CTA of the cluster before
+// the pass's cluster barrier; every CTA then adds the C slice totals in rank order.  A draw finds the slice, then the tile where the inverse CDF
 // crosses its target; that CTA repeats the tile's scan and walks the crossing lane's 8
 // elements.  Weights are fp32 (R_k from p, q and c_k); totals, c_k and thresholds are
 // fp64 (this part's fp64 rate is too low for fp64 per element).
@@ -192,8 +192,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
   __shared__ int32_t s_par[kMaxNodes], s_x[kMaxNodes];
   __shared__ double s_S[kMaxNodes + 1];  // S_0 .. S_k of the current node
   __shared__ double s_tile[kMaxTiles];
-  __shared__ double s_total, s_pub[2];   // slice total; published, by pass parity
-  __shared__ int32_t s_last, s_pub_last[2];
+  __shared__ double s_total;
+  __shared__ int32_t s_last;
+  // Every rank's slice total and last element with weight, stored here by that rank
+  // before the pass's cluster barrier; two sets, by pass parity.
+  __shared__ double s_pub[2][kMaxCluster];
+  __shared__ int32_t s_pub_last[2][kMaxCluster];
   __shared__ int32_t s_bad, s_accept, s_tile_hit, s_found;
   __shared__ double s_target, s_before;
   pdl_wait_prior_grid();  // inputs written by the previous kernel in the stream are visible
@@ -228,16 +232,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
   // totals added in rank order), and the row's last element with weight in *last.
   auto cluster_pass = [&](const float* pu, const float* qu, float c, int* last) -> double {
     const double mine = pass_totals(pu, qu, xb, xe, c, s_tile, &s_last, &s_total);
-    if (tid == 0) {
-      s_pub[pp] = mine;
-      s_pub_last[pp] = s_last;
+    if (tid < C) {  // this slice's total into every rank of the cluster
+      *cluster.map_shared_rank(&s_pub[pp][rank], tid) = mine;
+      *cluster.map_shared_rank(&s_pub_last[pp][rank], tid) = s_last;
     }
-    cluster.sync();  // every slice total of this pass is published
+    cluster.sync();  // every slice total of this pass is here
     double all = 0.0;
     int lst = -1;
     for (int r = 0; r < C; ++r) {
-      all += *cluster.map_shared_rank(&s_pub[pp], r);
-      lst = max(lst, *cluster.map_shared_rank(&s_pub_last[pp], r));
+      all += s_pub[pp][r];
+      lst = max(lst, s_pub_last[pp][r]);
     }
     pp ^= 1;
     *last = lst;
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
         double c = 0.0;
         int owner = -1;
         for (int r = 0; r < C; ++r) {
-          const double t = *cluster.map_shared_rank(&s_pub[pp ^ 1], r);
+          const double t = s_pub[pp ^ 1][r];
           if (owner < 0 && c + t > target) owner = r;
           if (owner < 0) c += t;
         }
@@ -348,11 +352,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
       }
     }
     __syncthreads();
-    if (tid == 0) s_pub_last[pp] = s_found;  // this CTA's find, for the cluster
+    if (tid < C) *cluster.map_shared_rank(&s_pub_last[pp][rank], tid) = s_found;  // for the cluster
     cluster.sync();
     if (rank == 0 && tid == 0) {
       int found = -1;
-      for (int r = 0; r < C; ++r) found = max(found, *cluster.map_shared_rank(&s_pub_last[pp], r));
+      for (int r = 0; r < C; ++r) found = max(found, s_pub_last[pp][r]);
       // Rounding can leave the target at or past the last crossing: the last token with
       // mass, as for the plain rule.
       const int drawn = total > 0.0 ? (found >= 0 ? found : last) : -1;
