@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
   const int n = a.n, V = a.V;
   const int xb = min(V, rank * a.slice), xe = min(V, xb + a.slice);  // this CTA's slice
   __shared__ int32_t s_par[kMaxNodes], s_x[kMaxNodes];
+  __shared__ float s_pux[kMaxNodes], s_qux[kMaxNodes];  // p_u, q_u at the child's token
   __shared__ double s_S[kMaxNodes + 1];  // S_0 .. S_k of the current node
   __shared__ double s_tile[kMaxTiles];
   __shared__ double s_total;
@@ -256,12 +257,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) spec_verify_tree_kernel(
     bool fallback = false;
     double ck = 0.0;  // c_k = S_0 + ... + S_{k-1} (every thread keeps the same sum)
     if (tid == 0) s_S[0] = 1.0;
+    // p_u and q_u at every child's token, loaded at once.
+    for (int i = u + tid; i < n; i += kThreads)
+      if (s_par[i] == u) {
+        s_pux[i] = pu[s_x[i]];
+        s_qux[i] = qu[s_x[i]];
+      }
+    __syncthreads();
     for (int c = u + 1; c <= n; ++c) {
       if (s_par[c - 1] != u) continue;
       if (tid == 0) {
-        const int x = s_x[c - 1];
-        const float qx = qu[x];
-        const double rx = fmax((double)pu[x] - ck * (double)qx, 0.0);
+        const float qx = s_qux[c - 1];
+        const double rx = fmax((double)s_pux[c - 1] - ck * (double)qx, 0.0);
         const uint4 w = philox4x32_10(make_uint4((uint32_t)(c - 1), (uint32_t)b, 0u, 0u),
                                       a.key0, a.key1);
         s_accept = philox_uniform(w.x) * s_S[k] * (double)qx <= rx;
