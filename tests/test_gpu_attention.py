@@ -54,6 +54,19 @@ def test_shapes_and_ragged_edges(vas_lib, D, P, Hq, Hkv, dtype):
     assert vas_lib.vas_last_device_error() == 0
 
 
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.FP8])
+def test_idle_slots(vas_lib, dtype):
+    """Batch slots with no context and no query (L = 0, ql = 0) between live sequences,
+    at the front and at the end: they get no work and leave their neighbours' rows alone."""
+    lens = [0, 37, 0, 0, 200, 16, 0, 1200, 0]
+    qlens = [0, 1, 0, 0, 5, 16, 0, 1, 0]
+    a = _case(lens, qlens, Hq=32, Hkv=8, D=128, P=16, dtype=dtype, seed=61)
+    ref_o, ref_l = oracle_attention(a)
+    out, lse = run_gpu_attention(vas_lib, to_device(a))
+    compare_attention(out, lse, ref_o, ref_l, dtype)
+    assert vas_lib.vas_last_device_error() == 0
+
+
 def test_row_blocks_beyond_64_rows(vas_lib):
     """GQA group 8 x 9 query tokens = 72 rows: two row blocks per KV head."""
     a = _case([300, 90, 1000], [9, 9, 1], Hq=64, Hkv=8, D=128, P=32, seed=11)
