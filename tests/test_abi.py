@@ -112,6 +112,41 @@ def test_host_validation_without_launch(vas_lib):
     assert lib.vas_status_string(vas_lib.VAS_E_WORKSPACE) == b"workspace too small"
 
 
+def test_host_validation_of_the_other_entry_points(vas_lib):
+    """spec_verify_tree, vas_philox4x32_10 and paged_attn_fwd_static refuse bad arguments
+    before any CUDA call."""
+    lib = vas_lib._lib
+    P = ctypes.c_void_p
+    fake, null = P(1 << 20), P(0)
+    tree = lambda B, n, V, p=fake, path=fake: lib.spec_verify_tree(p, fake, fake, fake, 1, fake,
+                                                                 fake, path, B, n, V, null)
+    assert tree(4, 0, 100) == vas_lib.VAS_E_INVALID_ARG      # no draft node
+    assert tree(4, 256, 100) == vas_lib.VAS_E_INVALID_ARG    # more nodes than 255
+    assert tree(-1, 4, 100) == vas_lib.VAS_E_INVALID_ARG
+    assert tree(4, 4, 0) == vas_lib.VAS_E_INVALID_ARG
+    assert tree(4, 4, 100, p=null) == vas_lib.VAS_E_INVALID_ARG
+    assert tree(4, 4, 100, path=null) == vas_lib.VAS_E_INVALID_ARG
+    assert tree(4, 1, 8 * 160 * 256 + 1) == vas_lib.VAS_E_UNSUPPORTED  # past 327680
+    assert tree(4, 255, 1 << 22) == vas_lib.VAS_E_INVALID_ARG  # (n + 1) V past int32 / 2
+    assert lib.spec_verify_tree(null, null, null, null, 1, null, null, null, 0, 4, 100,
+                                null) == vas_lib.VAS_OK      # empty batch
+    ph = lib.vas_philox4x32_10
+    assert ph(fake, 1, 2, fake, -1, null) == vas_lib.VAS_E_INVALID_ARG
+    assert ph(null, 1, 2, fake, 8, null) == vas_lib.VAS_E_INVALID_ARG
+    assert ph(P((1 << 20) + 4), 1, 2, fake, 8, null) == vas_lib.VAS_E_INVALID_ARG
+    assert ph(null, 1, 2, null, 0, null) == vas_lib.VAS_OK
+    st = lib.paged_attn_fwd_static
+    st.argtypes = [P] * 8 + [ctypes.POINTER(vas_lib.vas_attn_dims), P]
+    st.restype = ctypes.c_int
+    assert st(fake, fake, fake, fake, fake, fake, fake, fake,
+              ctypes.byref(_dims(vas_lib, head_dim=80)), null) == vas_lib.VAS_E_UNSUPPORTED
+    assert st(fake, fake, fake, fake, fake, fake, fake, fake,
+              ctypes.byref(_dims(vas_lib, num_q_heads=33)), null) == vas_lib.VAS_E_INVALID_ARG
+    big = _dims(vas_lib, num_seqs=2_000_000, total_q_tokens=2_000_000)
+    assert st(fake, fake, fake, fake, fake, fake, fake, fake, ctypes.byref(big),
+              null) == vas_lib.VAS_E_WORKSPACE               # past the 32 MiB array
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     """The product package raises when libvas.so is absent instead of falling back."""
     import subprocess
