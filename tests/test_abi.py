@@ -147,6 +147,43 @@ def test_host_validation_of_the_other_entry_points(vas_lib):
               null) == vas_lib.VAS_E_WORKSPACE               # past the 32 MiB array
 
 
+def test_product_path_never_reaches_the_oracle():
+    """Nothing in the package imports, loads or runs the oracle, and the oracle imports
+    nothing from the CUDA path: the two share only the input generators."""
+    import ast
+    pkg = os.path.join(ROOT, "verify_attention_spec_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            path = os.path.join(dirpath, f)
+            if f.endswith(".py"):
+                tree = ast.parse(open(path).read())
+                for node in ast.walk(tree):
+                    if isinstance(node, ast.Import):
+                        names = [n.name for n in node.names]
+                    elif isinstance(node, ast.ImportFrom):
+                        names = [node.module or ""]
+                    else:
+                        continue
+                    assert not any(n.split(".")[0] == "oracle" for n in names), path
+                text = open(path).read()
+                assert "liboracle" not in text and "oracle.c" not in text, path
+            elif f.endswith((".cu", ".cuh", ".cpp", ".h")):
+                assert "oracle" not in open(path).read().lower(), path
+    odir = os.path.join(ROOT, "oracle")
+    for f in os.listdir(odir):
+        path = os.path.join(odir, f)
+        if f.endswith(".py"):
+            for node in ast.walk(ast.parse(open(path).read())):
+                if isinstance(node, (ast.Import, ast.ImportFrom)):
+                    names = ([n.name for n in node.names] if isinstance(node, ast.Import)
+                             else [node.module or ""])
+                    assert not any(n.startswith("verify_attention_spec_gb300") for n in names), f
+            assert "libvas" not in open(path).read(), f
+        elif f.endswith((".c", ".h")):
+            includes = [l for l in open(path) if l.lstrip().startswith("#include")]
+            assert not any("vas" in l or "csrc" in l for l in includes), f
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     """The product package raises when libvas.so is absent instead of falling back."""
     import subprocess
