@@ -6,8 +6,14 @@
  *                     speculative-verify (k+1 query tokens) sequences over a KV cache
  *                     held in fixed-size pages addressed through per-sequence block
  *                     tables (split-KV with a log-sum-exp merge).
+ *   paged_attn_fwd_tree, paged_attn_fwd_quant, paged_attn_fwd_static : the same
+ *                     attention with draft-tree masks, over FP8 / INT8 pages, and
+ *                     without a caller workspace.
  *   spec_verify     : speculative-decoding modified rejection sampling with an
- *                     in-kernel Philox4x32-10 stream.
+ *                     in-kernel Philox4x32-10 stream; spec_verify_tree, the same rule
+ *                     over a draft tree.
+ *   vas_last_device_error, vas_philox4x32_10 : the device error word, and the device
+ *                     Philox stream on caller counters.
  *   vas_pool_*      : host-side page allocator and block-table builder that models
  *                     admission, growth, rollback of rejected drafts, eviction.
  *
