@@ -97,3 +97,29 @@ def test_ncu_traffic_is_dropped_when_the_kernel_source_changed(tmp_path, monkeyp
     assert bench.ncu_traffic("other") is None
     (csrc / bench.KERNEL_SOURCES["paged_attn"][0]).write_text("// changed\n")
     assert bench.ncu_traffic("w") is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` times the oracle on the host cores (no GPU needed) and
+    prints one JSON line with the contract's keys; under a launcher only rank 0 prints."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload",
+           "tiny", "--steps", "2", "--warmup", "1"]
+    env = dict(os.environ, RANK="0")
+    out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600, check=True)
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["value"] == d["value"] and d["e2e"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    other = subprocess.run(cmd, capture_output=True, text=True, env=dict(os.environ, RANK="1"),
+                           timeout=600, check=True)
+    assert other.stdout.strip() == ""
