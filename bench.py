@@ -178,8 +178,12 @@ class ClockSampler:
                  "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
             time.sleep(0.15)
-        except Exception:
+        except Exception:  # no nvidia-smi: the line says the clocks were unavailable
             self.proc = None
+            if getattr(self, "f", None) is not None:
+                self.f.close()
+            if self.path and os.path.exists(self.path):
+                os.unlink(self.path)
 
     def stop(self):
         if self.proc is None:

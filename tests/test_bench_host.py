@@ -123,3 +123,28 @@ def test_reference_arm_prints_one_contract_line():
     other = subprocess.run(cmd, capture_output=True, text=True, env=dict(os.environ, RANK="1"),
                            timeout=600, check=True)
     assert other.stdout.strip() == ""
+
+
+def test_clock_sampler_reads_clocks_and_throttle_reasons(tmp_path, monkeypatch):
+    """The sampler takes the median SM clock, the highest maximum clock and every
+    throttle reason seen Active, from nvidia-smi's CSV (a stand-in script here)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "echo '1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '2010, 2070, 1200.5, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '[N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    s.start()
+    import time
+    time.sleep(0.5)
+    got = s.stop()
+    assert got == {"sm_mhz": 2010.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+    monkeypatch.setenv("PATH", str(tmp_path / "empty"))
+    s = bench.ClockSampler(0)
+    s.start()
+    assert s.stop()["reasons"] == ["unavailable"]
