@@ -148,3 +148,27 @@ def test_clock_sampler_reads_clocks_and_throttle_reasons(tmp_path, monkeypatch):
     s = bench.ClockSampler(0)
     s.start()
     assert s.stop()["reasons"] == ["unavailable"]
+
+
+def test_kv_bytes_match_the_pages_worked_example():
+    """The bench's KV byte count for one layer, times the layers, gives the per-token and
+    per-context cache sizes the pages work out (tests/golden/kv_cache_bytes_per_token.txt)."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                        "kv_cache_bytes_per_token.txt")
+    g = {}
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = (x.strip() for x in line.split("="))
+            g[k] = float(v)
+    layers, H, D = int(g["layers"]), int(g["kv_heads"]), int(g["head_dim"])
+    e, ctx = int(g["bytes_per_element"]), int(g["context_tokens"])
+    P = 16
+    # one layer, one sequence of ctx tokens with no query rows: KV plus the block table
+    one_layer = bench.attn_bytes([ctx], [0], Hq=H, Hkv=H, D=D, P=P, elem=e)
+    kv_layer = one_layer - (ctx + P - 1) // P * 4
+    per_token = kv_layer // ctx * layers
+    assert per_token == 2 * layers * H * D * e == 2_621_440
+    assert abs(per_token / 1e6 - g["per_token_mb_printed"]) < 0.05
+    per_context = per_token * ctx
+    assert abs(per_context / 1e9 - g["per_context_gb_printed"]) < 0.8  # 10.7 GB: "about 10"
